@@ -1,0 +1,2 @@
+"""CPU oracle (test infrastructure only; never imported by the product path)."""
+from .muon_oracle import *  # noqa: F401,F403
