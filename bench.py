@@ -1,0 +1,464 @@
+"""Benchmark of the one-GPU Muon step: NS-orthogonalised matrices/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one muon_step over one copy of the workload's parameter groups:
+momentum update + BF16 cast, Newton-Schulz on every matrix, weight update.
+Inputs are seeded synthetic tensors resident in HBM and larger than L2, so
+no flush is needed between steps.  With N > 1 (torchrun) every rank steps
+its own copy of the workload (independent matrices, no exchange), and the
+job value is all ranks' matrices over the slowest rank's time.
+
+The JSON line adds the roofline of the dominant kernel (the Newton-Schulz
+update product), measured live with CUDA events on the launching stream,
+the CPU oracle timed on a bounded sample (rank 0, N = 1), and an
+end-to-end figure through the host-buffer entry point with the copies
+inside the timed region.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NS-orthogonalised matrices/s and TFLOPS (% of GB300 BF16 peak); muon_step ms"
+UNIT = "matrices/s"
+DEFAULT_WORKLOAD = "l24_attention"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DOMINANT = "ns_update"
+NS_SOURCES = ("newton_schulz_03_gb300/csrc/k_ns_gemm.cu", "newton_schulz_03_gb300/csrc/sm103_ptx.cuh")
+
+
+# ----------------------------------------------------------------- harness
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def timed_steps(step, steps: int, warmup: int, world: int, stream, sync) -> float:
+    """W untimed steps, then K steps between barrier+sync on both sides,
+    timed with CUDA events on `stream`.  Returns seconds (max over ranks)."""
+    import torch
+    for _ in range(warmup):
+        step()
+    sync()
+    barrier(world)
+    sync()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    sync()
+    barrier(world)
+    secs = e0.elapsed_time(e1) / 1e3
+    return max_over_ranks(secs, world, device=torch.device("cuda", torch.cuda.current_device()))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"muon_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "power_w_max": max(r[2] for r in rows),
+                "samples": len(loaded), "reasons": reasons}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def ns_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in NS_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{DOMINANT}_{workload.split('[')[0]}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha256_16") != ns_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------- our arm
+def capped(w, max_count):
+    """The workload with every group's count capped (small profiling cases)."""
+    if not max_count:
+        return w
+    import dataclasses
+    gs = tuple(dataclasses.replace(g, count=min(g.count, max_count)) for g in w.groups)
+    return dataclasses.replace(w, name=f"{w.name}[count<={max_count}]", groups=gs)
+
+
+def workload_groups(w):
+    return [(g.rows, g.cols, g.count) for g in w.groups]
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import newton_schulz_03_gb300 as ns
+    from newton_schulz_03_gb300.workloads import WORKLOADS, make_group_torch
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    w = capped(WORKLOADS[args.workload], args.max_count)
+    groups = workload_groups(w)
+    tensors = [make_group_torch(w, gi, dev) for gi in range(len(w.groups))]
+    Ws = [t[0] for t in tensors]
+    Ms = [t[1] for t in tensors]
+    Gs = [t[2] for t in tensors]
+    del tensors
+    stream = torch.cuda.current_stream()
+    handle = ns.Handle(device=local)
+    h = handle.value
+    plan = ns.muon_plan_describe(groups, w.ns_steps)
+    layers = w.layers
+
+    def step():
+        # One step of the workload: `layers` calls over the resident layer.
+        for _ in range(layers):
+            ns.muon_step(h, groups, Ms, Gs, Ws, w.lr, w.wd, w.mu, w.ns_steps, stream)
+
+    sync = torch.cuda.synchronize
+    step()
+    ns.muon_last_device_error(h, stream)
+    ns.muon_reset_kernel_stats(h)
+
+    with ClockSampler(local) as clk:
+        ns.muon_set_kernel_timing(h, True)
+        ns.muon_reset_kernel_stats(h)
+        launches0 = ns.muon_kernel_stats(h)["total_launches"]
+        secs = timed_steps(step, args.steps, args.warmup, world, stream, sync)
+        stats = ns.muon_kernel_stats(h)
+        ns.muon_set_kernel_timing(h, False)
+    ns.muon_last_device_error(h, stream)
+    clocks = clk.summary()
+    # Launch and time counts include the warm-up steps; scale to the timed K.
+    frac_timed = args.steps / float(args.steps + args.warmup)
+    gpu_launches = int(round((stats["total_launches"] - launches0) * frac_timed))
+
+    matrices_per_step = w.matrices
+    value = world * matrices_per_step * args.steps / secs
+    ms_per_step = secs * 1e3 / args.steps
+    flops_step = plan["ns_algorithmic_flops"] * layers
+    tflops = world * flops_step * args.steps / secs / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    # Dominant kernel: the update product X' = aX + BX, 2 m^2 n flops per matrix.
+    upd_flops_step = sum(c * 2.0 * mm * mm * nn for (mm, nn), c in w.wide_batches().items()) \
+        * w.ns_steps * layers
+    upd_launches = stats["launches"][DOMINANT]
+    upd_ms = stats["total_ms"][DOMINANT]
+    steps_recorded = args.steps + args.warmup
+    achieved = (upd_flops_step * steps_recorded) / (upd_ms / 1e3) / 1e12 if upd_ms > 0 else None
+    ns_ms = sum(stats["total_ms"][k] for k in ("ns_gram", "ns_poly", "ns_update"))
+    ns_tflops = (flops_step * steps_recorded) / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
+    kernel_share = {k: round(v / max(sum(stats["total_ms"].values()), 1e-9), 4)
+                    for k, v in stats["total_ms"].items() if v > 0}
+    traffic = profiled_traffic(w.name)
+    roofline = {
+        "kernel": "ns_gemm_kernel<update,256> (X' = a X + B X)",
+        "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
+        "peak": peak, "unit": "TFLOP/s",
+        "frac": round(achieved / peak, 4) if achieved else None,
+        "peak_source": f"{peak_src} bf16_tflops_sustained (of {peak_src})",
+        "frac_of_burst": round(achieved / burst, 4) if achieved else None,
+        "traffic": traffic,
+        "launches": upd_launches,
+        "avg_launch_ms": round(upd_ms / upd_launches, 4) if upd_launches else None,
+        "ns_engine_tflops": round(ns_tflops, 1) if ns_tflops else None,
+        "ns_engine_frac": round(ns_tflops / peak, 4) if ns_tflops else None,
+        "kernel_time_share": kernel_share,
+    }
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch RNG on device, shapes of the workload)",
+        "config": {
+            "workload": w.name, "description": w.description,
+            "matrices_per_step": matrices_per_step, "groups": groups, "layers": layers,
+            "ns_steps": w.ns_steps, "mu": w.mu, "lr": w.lr, "wd": w.wd,
+            "precision": "FP32 momentum and weights, BF16 Newton-Schulz with FP32 accumulation",
+            "l2": "inputs larger than L2 (%.1f GB of FP32 state per layer), no flush"
+                  % (sum(g.numel for g in w.groups) * 12 / 1e9),
+            "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
+        },
+        "tflops_algorithmic": round(tflops, 1),
+        "pct_of_bf16_peak": round(100 * tflops / peak, 2),
+        "tflops_dense_equivalent": round(tflops * dense_over_alg(w), 1),
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "roofline": roofline,
+    }
+    if not args.skip_e2e:
+        line["e2e"] = run_e2e(args, ns, h, w, groups, Ws, Ms, Gs, world)
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        del Ws, Ms, Gs
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    handle.close()
+    return line
+
+
+def dense_over_alg(w) -> float:
+    alg = dense = 0.0
+    for (m, n), c in w.wide_batches().items():
+        alg += c * (3.0 * m * m * n + m ** 3)
+        dense += c * (4.0 * m * m * n + 2.0 * m ** 3)
+    return dense / alg
+
+
+def run_e2e(args, ns, h, w, groups, Ws, Ms, Gs, world):
+    """The same step through muon_step_host: pinned host buffers, H2D of
+    momentum, gradient and weights and D2H of momentum and weights inside
+    the timed region."""
+    import torch
+    hW = [t.cpu().pin_memory() for t in Ws]
+    hM = [t.cpu().pin_memory() for t in Ms]
+    hG = [t.cpu().pin_memory() for t in Gs]
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for _ in range(w.layers):
+            ns.muon_step_host(h, groups, hM, hG, hW, w.lr, w.wd, w.mu, w.ns_steps, stream)
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(1):
+        step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    secs = max_over_ranks(time.perf_counter() - t0, world,
+                          device=torch.device("cuda", torch.cuda.current_device()))
+    nbytes = sum(g.numel for g in w.groups) * 4 * w.layers
+    return {"value": round(world * w.matrices * steps / secs, 3), "unit": UNIT,
+            "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
+            "steps": steps, "ms_per_step": round(secs * 1e3 / steps, 3),
+            "api": "muon_step_host (pinned host buffers)"}
+
+
+# ----------------------------------------------------------------- CPU oracle
+def cpu_cores() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_sample_step(w, sample_matrices: int, seed_offset: int = 0):
+    """Run the oracle on `sample_matrices` matrices drawn from the workload's
+    groups (round robin over groups).  Returns (matrices, seconds)."""
+    import numpy as np
+
+    from oracle import muon_oracle as o
+    rng = np.random.default_rng(12345 + seed_offset)
+    done = 0
+    t0 = time.perf_counter()
+    gi = 0
+    while done < sample_matrices:
+        g = w.groups[gi % len(w.groups)]
+        gi += 1
+        W = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.w_std))
+        M = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.m_std))
+        G = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.g_std))
+        o.muon_step_matrix(W, M, G, lr=w.lr, wd=w.wd, mu=w.mu, ns_steps=w.ns_steps)
+        done += 1
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(w, seconds_budget: float):
+    # Size the sample from one timed matrix so the leg takes ~seconds_budget.
+    n1, t1 = oracle_sample_step(w, 1, 0)
+    k = max(1, min(64, int(seconds_budget / max(t1, 1e-3)) - 1))
+    nk, tk = oracle_sample_step(w, k, 1)
+    n, t = n1 + nk, t1 + tk
+    shapes = sorted({f"{g.rows}x{g.cols}" for g in w.groups})
+    return {"value": round(n / t, 4), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} matrices ({', '.join(shapes)}) of workload {w.name}, FP64 NumPy "
+                      f"oracle, {t:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm (rank 0 only)."""
+    from newton_schulz_03_gb300.workloads import WORKLOADS
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    # Size one step to a bounded sample so the whole run takes minutes.
+    n1, t1 = oracle_sample_step(w, 1, 0)
+    total_budget = 150.0
+    per_step = max(1, int(total_budget / (args.steps + args.warmup) / max(t1, 1e-3)))
+    per_step = min(per_step, w.matrices)
+    for i in range(args.warmup):
+        oracle_sample_step(w, per_step, 100 + i)
+    done = 0
+    secs = 0.0
+    for i in range(args.steps):
+        n, t = oracle_sample_step(w, per_step, 1000 + i)
+        done += n
+        secs += t
+    value = done / secs
+    shapes = sorted({f"{g.rows}x{g.cols}" for g in w.groups})
+    sample = (f"{per_step} matrices per step ({', '.join(shapes)}) of workload {w.name}, "
+              f"FP64 NumPy oracle")
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": w.name, "matrices_per_step_sampled": per_step,
+                   "note": "CPU oracle on a bounded sample of the workload"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--max-count", type=int, default=0,
+                    help="cap every group's matrix count (small profiling cases)")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,213 @@
+/*
+ * muon.h -- C ABI of the one-GPU Muon optimiser step for GB300 (sm_103a).
+ *
+ * The step is the local part of the distributed Muon update described in
+ * "Frontier Pre-training at Microsoft AI" (papercache deepnotes summary),
+ * Method details §5 "Scaling Muon to 16K GPUs", resharding steps 1, 3 and 5,
+ * and in "Microsoft Reveals MAI-Base-2 Training Recipe" (xiaohu-jiedu),
+ * section "How to Make Parameter Updates Faster and More Stable?":
+ *   1. update the FP32 momentum in place and cast it to BF16;
+ *   2. batch parameters of identical shape;
+ *   3. orthogonalise every whole momentum matrix with a symmetry-aware
+ *      Newton-Schulz operator;
+ *   4. cast the result back to FP32 and apply it to the FP32 weights.
+ * The two all-to-all exchanges between the steps move data between GPUs
+ * and are not part of this one-GPU library.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named *_dev are CUDA device pointers owned by the caller; the
+ *    library never frees them.  Pointers named *_host are host pointers.
+ *  - Matrices are dense, row-major and contiguous.  A group of `count`
+ *    matrices of rows x cols is one buffer of count*rows*cols elements.
+ *  - "Wide" layout: a matrix with rows > cols is orthogonalised as its
+ *    transpose, so the BF16 working copy of every matrix is m x n with
+ *    m = min(rows, cols) <= n = max(rows, cols).
+ *  - BF16 values travel as uint16_t bit patterns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously; no entry point synchronises
+ *    the stream unless it says so.
+ *  - Arguments are validated on the host before anything is enqueued: an
+ *    invalid argument returns MUON_ERR_INVALID_ARG and launches nothing.
+ *  - A handle is bound to the device that was current when it was created
+ *    and is not thread-safe.
+ *  - Kernels report device-side failures (a bounded wait that expired, a
+ *    non-finite norm) through a flag read by muon_last_device_error().
+ */
+#ifndef MUON_GB300_H_
+#define MUON_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MUON_OK = 0,
+  MUON_ERR_INVALID_ARG = 1,       /* bad pointer, size, count or value */
+  MUON_ERR_NOMEM = 2,             /* workspace allocation failed */
+  MUON_ERR_CUDA = 3,              /* a CUDA runtime/driver call failed */
+  MUON_ERR_UNSUPPORTED_ARCH = 4,  /* device is not compute capability 10.3 */
+  MUON_ERR_TIMEOUT = 5,           /* a bounded device-side wait expired */
+  MUON_ERR_NONFINITE = 6,         /* a momentum norm was NaN or Inf */
+  MUON_ERR_NO_DEVICE = 7          /* no CUDA device is visible */
+} muon_status_t;
+
+typedef struct muon_handle_s* muon_handle_t;
+
+/* One group of same-shape parameters ("Scaling Muon to 16K GPUs",
+ * resharding step 2: parameters of identical shape are batched).
+ * `update_scale` multiplies the orthogonalised update (1.0 = plain step). */
+typedef struct {
+  int32_t rows;
+  int32_t cols;
+  int32_t count;
+  float update_scale;
+} muon_group_t;
+
+/* Kernel classes, for timing and launch accounting. */
+typedef enum {
+  MUON_KERNEL_MOMENTUM_CAST = 0,  /* momentum update + BF16 cast + transpose */
+  MUON_KERNEL_NORM = 1,           /* per-matrix Frobenius norm finalisation */
+  MUON_KERNEL_NS_GRAM = 2,        /* A = alpha X X^T (upper tiles + mirror) */
+  MUON_KERNEL_NS_POLY = 3,        /* B = b A + c A A (upper tiles + mirror) */
+  MUON_KERNEL_NS_UPDATE = 4,      /* X' = alpha (a X + B X) */
+  MUON_KERNEL_APPLY = 5,          /* W = W (1 - lr wd) - lr s O */
+  MUON_KERNEL_SCALE = 6,          /* ns_steps == 0: O = X / s */
+  MUON_KERNEL_COUNT = 7
+} muon_kernel_t;
+
+typedef struct {
+  double total_ms[MUON_KERNEL_COUNT];   /* summed device time per class */
+  int64_t launches[MUON_KERNEL_COUNT];  /* launches per class */
+  int64_t total_launches;               /* all kernel launches of the handle */
+} muon_kernel_stats_t;
+
+/* Plan summary of a group list (pure host computation, no GPU needed). */
+typedef struct {
+  int32_t n_batches;          /* distinct wide shapes (Newton-Schulz batches) */
+  int32_t n_chunks;           /* batch chunks that fit the workspace */
+  int32_t max_chunk_matrices; /* largest chunk */
+  int64_t matrices;           /* total matrices */
+  size_t workspace_bytes;     /* device workspace the plan needs */
+  double ns_algorithmic_flops;/* sum over matrices of ns_steps*(3 m^2 n + m^3) */
+  int64_t launches_per_step;  /* kernel launches one muon_step makes */
+} muon_plan_info_t;
+
+/* Default Newton-Schulz configuration: quintic coefficients (a, b, c),
+ * 5 iterations and the epsilon added to the Frobenius norm. */
+#define MUON_NS_A 3.4445f
+#define MUON_NS_B (-4.7750f)
+#define MUON_NS_C 2.0315f
+#define MUON_NS_STEPS 5
+#define MUON_NORM_EPS 1e-7f
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* muon_status_string(muon_status_t status);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+const char* muon_last_error_message(void);
+
+/* Library version string. */
+const char* muon_version(void);
+
+/* Create a handle on `device` (-1 = the calling thread's current device).
+ * `workspace_bytes_max` caps the device workspace the handle may allocate
+ * (0 = default of 8 GiB); groups whose whole batch does not fit are
+ * processed in chunks.  No device memory is allocated until first use.
+ * Errors: INVALID_ARG (out == NULL), NO_DEVICE, UNSUPPORTED_ARCH (not
+ * sm_103), CUDA. */
+muon_status_t muon_create(muon_handle_t* out, int32_t device, size_t workspace_bytes_max);
+
+/* Destroy a handle and free its workspace (synchronises the device). */
+muon_status_t muon_destroy(muon_handle_t handle);
+
+/* Plan of a group list under a workspace cap, without a GPU.
+ * Same group rules as muon_step.  Errors: INVALID_ARG. */
+muon_status_t muon_plan_describe(const muon_group_t* groups, int32_t n_groups,
+                                 int32_t ns_steps, size_t workspace_bytes_max,
+                                 muon_plan_info_t* out);
+
+/* The whole Muon step on device buffers ("Scaling Muon to 16K GPUs",
+ * resharding steps 1, 3, 5; "How to Make Parameter Updates Faster and More
+ * Stable?").  For every matrix of every group:
+ *   M  <- mu * M + G                          (FP32, in place)
+ *   X  <- bf16_rne(M), transposed if rows > cols
+ *   s  <- ||M||_F + 1e-7
+ *   X  <- X / s; then ns_steps times: A = X X^T; B = b A + c A^2;
+ *         X = a X + B X                       (BF16 operands, FP32 accumulate)
+ *   W  <- W (1 - lr*wd) - lr * update_scale * fp32(X), transposed back
+ * groups:          [n_groups] host array; rows, cols >= 1; count >= 0.
+ * momentum_dev:    [n_groups] host array of device pointers, FP32 in/out.
+ * grad_dev:        [n_groups] host array of device pointers, FP32 read-only.
+ * weights_dev:     [n_groups] host array of device pointers, FP32 in/out.
+ * ns_steps:        0..64 (0 applies the normalised BF16 momentum).
+ * The three buffers of a group must not overlap each other.
+ * Same-wide-shape groups share one Newton-Schulz batch.
+ * Errors: INVALID_ARG (NULL pointer with count > 0, bad sizes, non-finite
+ * lr/wd/mu, unaligned pointer: 16-byte alignment is required), NOMEM, CUDA. */
+muon_status_t muon_step(muon_handle_t handle, const muon_group_t* groups, int32_t n_groups,
+                        float* const* momentum_dev, const float* const* grad_dev,
+                        float* const* weights_dev, float lr, float wd, float mu,
+                        int32_t ns_steps, void* stream);
+
+/* The same step on HOST buffers: copies momentum, gradient and weights to
+ * device staging owned by the handle, runs muon_step, copies momentum and
+ * weights back, and synchronises `stream` before returning.  Pinned host
+ * memory gives asynchronous copies.  Staging is grown on demand. */
+muon_status_t muon_step_host(muon_handle_t handle, const muon_group_t* groups, int32_t n_groups,
+                             float* const* momentum_host, const float* const* grad_host,
+                             float* const* weights_host, float lr, float wd, float mu,
+                             int32_t ns_steps, void* stream);
+
+/* Step 1 alone: momentum update, BF16 cast into wide layout, and the
+ * per-matrix inverse scale 1/(||M||_F + 1e-7).
+ * momentum_dev:  count*rows*cols FP32, updated in place.
+ * grad_dev:      count*rows*cols FP32.
+ * x_wide_dev:    count*m*n BF16 output (m = min, n = max of rows, cols).
+ * inv_norm_dev:  count FP32 output. */
+muon_status_t muon_momentum_cast(muon_handle_t handle, int32_t rows, int32_t cols, int32_t count,
+                                 float* momentum_dev, const float* grad_dev, float mu,
+                                 uint16_t* x_wide_dev, float* inv_norm_dev, void* stream);
+
+/* Step 3 alone: batched symmetric Newton-Schulz on `count` wide BF16
+ * matrices m x n (m <= n), each pre-scaled by inv_norm[i]:
+ *   X0 = inv_norm[i] * x[i]; ns_steps times X = a X + (b A + c A^2) X,
+ *   A = X X^T.  Gram and square products compute only upper-triangle
+ *   tiles and mirror them.
+ * x_dev, out_dev: count*m*n BF16, 16-byte aligned, must not overlap.
+ * inv_norm_dev:   count FP32 (device).
+ * coeffs_host:    3 floats (a, b, c) or NULL for the defaults.
+ * m and n must be multiples of 8 (row pitch of 16 bytes for the tensor
+ * memory accelerator).  Errors: INVALID_ARG, NOMEM, CUDA. */
+muon_status_t muon_newton_schulz_bf16(muon_handle_t handle, int32_t m, int32_t n, int32_t count,
+                                      const uint16_t* x_dev, uint16_t* out_dev,
+                                      const float* inv_norm_dev, int32_t ns_steps,
+                                      const float* coeffs_host, void* stream);
+
+/* Step 5 alone: W <- W (1 - lr*wd) - lr*scale*fp32(O), O given in wide
+ * layout (transposed back when rows > cols).
+ * weights_dev: count*rows*cols FP32 in/out; o_wide_dev: count*m*n BF16. */
+muon_status_t muon_apply_update(muon_handle_t handle, int32_t rows, int32_t cols, int32_t count,
+                                float* weights_dev, const uint16_t* o_wide_dev,
+                                float lr, float wd, float scale, void* stream);
+
+/* Synchronise `stream`, then read and clear the handle's device error
+ * flag: MUON_OK, MUON_ERR_TIMEOUT or MUON_ERR_NONFINITE. */
+muon_status_t muon_last_device_error(muon_handle_t handle, void* stream);
+
+/* Per-kernel timing: when enabled, every launch is bracketed by CUDA
+ * events on the launching stream.  muon_kernel_stats synchronises the
+ * device, folds the recorded events into `out` and keeps accumulating;
+ * muon_reset_kernel_stats clears the totals. */
+muon_status_t muon_set_kernel_timing(muon_handle_t handle, int32_t enable);
+muon_status_t muon_kernel_stats(muon_handle_t handle, muon_kernel_stats_t* out);
+muon_status_t muon_reset_kernel_stats(muon_handle_t handle);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MUON_GB300_H_ */

@@ -1,0 +1,24 @@
+"""One-GPU Muon optimiser step for GB300 (sm_103a).
+
+The compute runs in hand-written CUDA kernels behind the C ABI of
+``include/muon.h``; this package is the ctypes binding (same function
+names) plus the synthetic workload definitions used by tests and the
+benchmark.
+"""
+
+from ._native import (  # noqa: F401
+    EXPORTED, KERNEL_NAMES, LIB_PATH, Handle, MuonError, load_library, muon_apply_update,
+    muon_create, muon_destroy, muon_kernel_stats, muon_last_device_error,
+    muon_last_error_message, muon_momentum_cast, muon_newton_schulz_bf16, muon_plan_describe,
+    muon_reset_kernel_stats, muon_set_kernel_timing, muon_status_string, muon_step,
+    muon_step_host, muon_version,
+)
+
+__all__ = [
+    "EXPORTED", "KERNEL_NAMES", "LIB_PATH", "Handle", "MuonError", "load_library",
+    "muon_apply_update", "muon_create", "muon_destroy", "muon_kernel_stats",
+    "muon_last_device_error", "muon_last_error_message", "muon_momentum_cast",
+    "muon_newton_schulz_bf16", "muon_plan_describe", "muon_reset_kernel_stats",
+    "muon_set_kernel_timing", "muon_status_string", "muon_step", "muon_step_host",
+    "muon_version",
+]

@@ -1,0 +1,271 @@
+"""ctypes binding of the C ABI in include/muon.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls.  Tensors
+are PyTorch tensors (device memory and streams come from PyTorch); the
+work itself runs in the library's CUDA kernels.  There is no fallback: if
+the shared library is missing or the device is not sm_103, calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, List, Optional, Sequence, Tuple, Union
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmuon_gb300.so")
+
+MUON_OK = 0
+STATUS_NAMES = {
+    0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_NOMEM", 3: "MUON_ERR_CUDA",
+    4: "MUON_ERR_UNSUPPORTED_ARCH", 5: "MUON_ERR_TIMEOUT", 6: "MUON_ERR_NONFINITE",
+    7: "MUON_ERR_NO_DEVICE",
+}
+KERNEL_NAMES = ("momentum_cast", "norm", "ns_gram", "ns_poly", "ns_update", "apply", "scale")
+N_KERNELS = len(KERNEL_NAMES)
+
+# Symbols the header declares (checked by the CPU test-suite).
+EXPORTED = (
+    "muon_status_string", "muon_last_error_message", "muon_version", "muon_create",
+    "muon_destroy", "muon_plan_describe", "muon_step", "muon_step_host", "muon_momentum_cast",
+    "muon_newton_schulz_bf16", "muon_apply_update", "muon_last_device_error",
+    "muon_set_kernel_timing", "muon_kernel_stats", "muon_reset_kernel_stats",
+)
+
+
+class MuonError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = STATUS_NAMES.get(status, f"status {status}")
+        super().__init__(f"{self.status_name}: {message}")
+
+
+class _Group(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int32), ("cols", ctypes.c_int32),
+                ("count", ctypes.c_int32), ("update_scale", ctypes.c_float)]
+
+
+class _Stats(ctypes.Structure):
+    _fields_ = [("total_ms", ctypes.c_double * N_KERNELS),
+                ("launches", ctypes.c_int64 * N_KERNELS),
+                ("total_launches", ctypes.c_int64)]
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("n_batches", ctypes.c_int32), ("n_chunks", ctypes.c_int32),
+                ("max_chunk_matrices", ctypes.c_int32), ("matrices", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t), ("ns_algorithmic_flops", ctypes.c_double),
+                ("launches_per_step", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load (once) the in-tree shared library; raise if it was not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build it with `python -m newton_schulz_03_gb300.build_lib`")
+    lib = ctypes.CDLL(p)
+    c_int, c_i32, c_f, c_vp, c_sz = ctypes.c_int, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "muon_status_string": (ctypes.c_char_p, [c_int]),
+        "muon_last_error_message": (ctypes.c_char_p, []),
+        "muon_version": (ctypes.c_char_p, []),
+        "muon_create": (c_int, [P(c_vp), c_i32, c_sz]),
+        "muon_destroy": (c_int, [c_vp]),
+        "muon_plan_describe": (c_int, [P(_Group), c_i32, c_i32, c_sz, P(_PlanInfo)]),
+        "muon_step": (c_int, [c_vp, P(_Group), c_i32, P(c_vp), P(c_vp), P(c_vp), c_f, c_f, c_f,
+                              c_i32, c_vp]),
+        "muon_step_host": (c_int, [c_vp, P(_Group), c_i32, P(c_vp), P(c_vp), P(c_vp), c_f, c_f,
+                                   c_f, c_i32, c_vp]),
+        "muon_momentum_cast": (c_int, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_f, c_vp, c_vp,
+                                       c_vp]),
+        "muon_newton_schulz_bf16": (c_int, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32,
+                                            P(c_f), c_vp]),
+        "muon_apply_update": (c_int, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_f, c_f, c_f,
+                                      c_vp]),
+        "muon_last_device_error": (c_int, [c_vp, c_vp]),
+        "muon_set_kernel_timing": (c_int, [c_vp, c_i32]),
+        "muon_kernel_stats": (c_int, [c_vp, P(_Stats)]),
+        "muon_reset_kernel_stats": (c_int, [c_vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != MUON_OK:
+        msg = load_library().muon_last_error_message().decode(errors="replace")
+        raise MuonError(status, msg)
+
+
+def _ptr(x) -> int:
+    """Address of a tensor / array / raw integer pointer."""
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_contiguous():
+            raise ValueError("tensors passed to the library must be contiguous")
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)!r}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return 0
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+GroupLike = Union[Tuple[int, int, int], Tuple[int, int, int, float]]
+
+
+def _groups(groups: Sequence[GroupLike]):
+    arr = (_Group * max(len(groups), 1))()
+    for i, g in enumerate(groups):
+        rows, cols, count = int(g[0]), int(g[1]), int(g[2])
+        scale = float(g[3]) if len(g) > 3 else 1.0
+        arr[i] = _Group(rows, cols, count, scale)
+    return arr
+
+
+def _ptr_array(xs: Sequence) -> ctypes.Array:
+    arr = (ctypes.c_void_p * max(len(xs), 1))()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x)
+    return arr
+
+
+# ---------------------------------------------------------------- entry points
+def muon_status_string(status: int) -> str:
+    return load_library().muon_status_string(status).decode()
+
+
+def muon_last_error_message() -> str:
+    return load_library().muon_last_error_message().decode(errors="replace")
+
+
+def muon_version() -> str:
+    return load_library().muon_version().decode()
+
+
+def muon_create(device: int = -1, workspace_bytes_max: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(load_library().muon_create(ctypes.byref(h), device, workspace_bytes_max))
+    return h.value
+
+
+def muon_destroy(handle: int) -> None:
+    _check(load_library().muon_destroy(handle))
+
+
+def muon_plan_describe(groups: Sequence[GroupLike], ns_steps: int = 5,
+                       workspace_bytes_max: int = 0) -> dict:
+    info = _PlanInfo()
+    _check(load_library().muon_plan_describe(_groups(groups), len(groups), ns_steps,
+                                             workspace_bytes_max, ctypes.byref(info)))
+    return {f: getattr(info, f) for f, _ in _PlanInfo._fields_}
+
+
+def muon_step(handle: int, groups: Sequence[GroupLike], momentum: Sequence, grad: Sequence,
+              weights: Sequence, lr: float, wd: float, mu: float, ns_steps: int = 5,
+              stream=None) -> None:
+    _check(load_library().muon_step(handle, _groups(groups), len(groups), _ptr_array(momentum),
+                                    _ptr_array(grad), _ptr_array(weights), lr, wd, mu, ns_steps,
+                                    _stream(stream)))
+
+
+def muon_step_host(handle: int, groups: Sequence[GroupLike], momentum: Sequence, grad: Sequence,
+                   weights: Sequence, lr: float, wd: float, mu: float, ns_steps: int = 5,
+                   stream=None) -> None:
+    _check(load_library().muon_step_host(handle, _groups(groups), len(groups),
+                                         _ptr_array(momentum), _ptr_array(grad),
+                                         _ptr_array(weights), lr, wd, mu, ns_steps,
+                                         _stream(stream)))
+
+
+def muon_momentum_cast(handle: int, rows: int, cols: int, count: int, momentum, grad, mu: float,
+                       x_wide, inv_norm, stream=None) -> None:
+    _check(load_library().muon_momentum_cast(handle, rows, cols, count, _ptr(momentum),
+                                             _ptr(grad), mu, _ptr(x_wide), _ptr(inv_norm),
+                                             _stream(stream)))
+
+
+def muon_newton_schulz_bf16(handle: int, m: int, n: int, count: int, x, out, inv_norm,
+                            ns_steps: int = 5, coeffs: Optional[Sequence[float]] = None,
+                            stream=None) -> None:
+    c = None
+    if coeffs is not None:
+        c = (ctypes.c_float * 3)(*[float(v) for v in coeffs])
+    _check(load_library().muon_newton_schulz_bf16(handle, m, n, count, _ptr(x), _ptr(out),
+                                                  _ptr(inv_norm), ns_steps, c, _stream(stream)))
+
+
+def muon_apply_update(handle: int, rows: int, cols: int, count: int, weights, o_wide,
+                      lr: float, wd: float, scale: float = 1.0, stream=None) -> None:
+    _check(load_library().muon_apply_update(handle, rows, cols, count, _ptr(weights),
+                                            _ptr(o_wide), lr, wd, scale, _stream(stream)))
+
+
+def muon_last_device_error(handle: int, stream=None) -> None:
+    _check(load_library().muon_last_device_error(handle, _stream(stream)))
+
+
+def muon_set_kernel_timing(handle: int, enable: bool) -> None:
+    _check(load_library().muon_set_kernel_timing(handle, 1 if enable else 0))
+
+
+def muon_kernel_stats(handle: int) -> dict:
+    st = _Stats()
+    _check(load_library().muon_kernel_stats(handle, ctypes.byref(st)))
+    return {"total_ms": {k: st.total_ms[i] for i, k in enumerate(KERNEL_NAMES)},
+            "launches": {k: st.launches[i] for i, k in enumerate(KERNEL_NAMES)},
+            "total_launches": st.total_launches}
+
+
+def muon_reset_kernel_stats(handle: int) -> None:
+    _check(load_library().muon_reset_kernel_stats(handle))
+
+
+class Handle:
+    """Owning wrapper: ``with Handle() as h: muon_step(h.value, ...)``."""
+
+    def __init__(self, device: int = -1, workspace_bytes_max: int = 0):
+        self.value = muon_create(device, workspace_bytes_max)
+
+    def close(self) -> None:
+        if self.value:
+            muon_destroy(self.value)
+            self.value = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,304 @@
+// k_elementwise.cu -- the HBM-bound steps of the Muon step on sm_103a.
+//
+//  * momentum_cast: "update the FP32 momentum shard in place, then cast it
+//    to BF16" (Frontier Pre-training at Microsoft AI, Method details §5,
+//    resharding step 1), fused with the transpose of tall matrices to the
+//    wide orientation and with per-tile partial sums of M^2 for the
+//    Frobenius pre-normalisation.  Traffic: read M, G; write M, X.
+//  * norm_finalize: deterministic per-matrix reduction of the partials.
+//  * apply_update: "cast the update back to FP32 and apply it to the
+//    weights" (same section, resharding step 5) with decoupled weight decay.
+//    Traffic: read W, O; write W.
+//  * scale_bf16: the degenerate zero-iteration case O = X / s.
+//
+// All four work on 64 x 64 tiles of the source matrix with 256 threads;
+// rows are read as float4 when the pitch allows it.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace muon {
+namespace {
+
+constexpr int T = kEwTile;   // 64
+constexpr int kThreads = 256;
+constexpr int kPad = 8;      // shared-memory row padding (bf16 elements)
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t u) {
+  return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
+
+template <typename Tv>
+__device__ __forceinline__ Tv block_sum(Tv v, Tv* red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  Tv s = 0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kThreads / 32; ++w) s += red[w];  // fixed order
+  }
+  return s;  // valid in thread 0
+}
+
+// grid = (tiles per matrix, count); tile = 64 source rows x 64 source cols.
+template <bool kTranspose>
+__global__ void __launch_bounds__(kThreads) momentum_cast_kernel(
+    int rows, int cols, float* __restrict__ M, const float* __restrict__ G, float mu,
+    uint16_t* __restrict__ X, int64_t x_ld, int64_t x_ms, float* __restrict__ partials) {
+  __shared__ __align__(16) uint16_t sT[kTranspose ? T : 1][T + kPad];
+  __shared__ float red[kThreads / 32];
+
+  const int tiles_c = (cols + T - 1) / T;
+  const int tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+  const int64_t mat = blockIdx.y;
+  const int64_t base = mat * static_cast<int64_t>(rows) * cols;
+  float* Mm = M + base;
+  const float* Gm = G + base;
+  uint16_t* Xm = X + mat * x_ms;
+
+  const int rr = threadIdx.x >> 4;        // 0..15
+  const int cc = (threadIdx.x & 15) * 4;  // 0..60
+  const bool vec_ok = (cols & 3) == 0;
+  float ss = 0.f;
+
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int lr_ = rr + 16 * i;
+    const int r = tr * T + lr_;
+    const int c = tc * T + cc;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < rows) {
+      const int64_t off = static_cast<int64_t>(r) * cols + c;
+      if (vec_ok && c + 3 < cols) {
+        float4 m4 = *reinterpret_cast<const float4*>(Mm + off);
+        const float4 g4 = __ldg(reinterpret_cast<const float4*>(Gm + off));
+        m4.x = fmaf(mu, m4.x, g4.x);
+        m4.y = fmaf(mu, m4.y, g4.y);
+        m4.z = fmaf(mu, m4.z, g4.z);
+        m4.w = fmaf(mu, m4.w, g4.w);
+        *reinterpret_cast<float4*>(Mm + off) = m4;
+        v[0] = m4.x; v[1] = m4.y; v[2] = m4.z; v[3] = m4.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (c + e < cols) {
+            const float mv = fmaf(mu, Mm[off + e], Gm[off + e]);
+            Mm[off + e] = mv;
+            v[e] = mv;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ss = fmaf(v[e], v[e], ss);
+    if constexpr (kTranspose) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sT[cc + e][lr_] = bf16_bits(v[e]);
+    } else if (r < rows) {
+      uint16_t* xr = Xm + static_cast<int64_t>(r) * x_ld + c;
+      if (c + 3 < cols && ((x_ld & 3) == 0)) {
+        uint2 p;
+        p.x = static_cast<uint32_t>(bf16_bits(v[0])) | (static_cast<uint32_t>(bf16_bits(v[1])) << 16);
+        p.y = static_cast<uint32_t>(bf16_bits(v[2])) | (static_cast<uint32_t>(bf16_bits(v[3])) << 16);
+        *reinterpret_cast<uint2*>(xr) = p;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c + e < cols) xr[e] = bf16_bits(v[e]);
+      }
+    }
+  }
+
+  if constexpr (kTranspose) {
+    __syncthreads();
+    // X (wide) row = source column, X column = source row.
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int idx = threadIdx.x + kThreads * j;  // 0..511
+      const int xrow_l = idx >> 3;                 // source column within tile
+      const int seg = (idx & 7) * 8;               // source rows seg..seg+7
+      const int xrow = tc * T + xrow_l;
+      const int xcol = tr * T + seg;
+      if (xrow < cols) {
+        uint16_t* dst = Xm + static_cast<int64_t>(xrow) * x_ld + xcol;
+        if (xcol + 7 < rows && ((x_ld & 7) == 0)) {
+          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&sT[xrow_l][seg]);
+        } else {
+          for (int e = 0; e < 8; ++e)
+            if (xcol + e < rows) dst[e] = sT[xrow_l][seg + e];
+        }
+      }
+    }
+  }
+
+  const float tot = block_sum(ss, red);
+  if (threadIdx.x == 0) partials[mat * gridDim.x + blockIdx.x] = tot;
+}
+
+__global__ void __launch_bounds__(kThreads) norm_finalize_kernel(
+    const float* __restrict__ partials, int per_matrix, float eps, float* __restrict__ inv_norm,
+    int* __restrict__ err) {
+  __shared__ double red[kThreads / 32];
+  const int64_t mat = blockIdx.x;
+  const float* p = partials + mat * per_matrix;
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < per_matrix; i += kThreads) acc += static_cast<double>(p[i]);
+  const double tot = block_sum(acc, red);
+  if (threadIdx.x == 0) {
+    if (!isfinite(tot)) {
+      atomicOr(err, kDevErrNonFinite);
+      inv_norm[mat] = 0.f;
+    } else {
+      inv_norm[mat] = static_cast<float>(1.0 / (sqrt(tot) + static_cast<double>(eps)));
+    }
+  }
+}
+
+// grid = (tiles per matrix of the weight, count); tile = 64 x 64 of W.
+template <bool kTranspose>
+__global__ void __launch_bounds__(kThreads) apply_update_kernel(
+    int rows, int cols, float* __restrict__ W, const uint16_t* __restrict__ O, int64_t o_ld,
+    int64_t o_ms, float lr, float wd, float scale) {
+  __shared__ __align__(16) uint16_t sO[kTranspose ? T : 1][T + kPad];
+  const int tiles_c = (cols + T - 1) / T;
+  const int tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+  const int64_t mat = blockIdx.y;
+  float* Wm = W + mat * static_cast<int64_t>(rows) * cols;
+  const uint16_t* Om = O + mat * o_ms;
+  const float decay = fmaf(-lr, wd, 1.0f);
+  const float step = lr * scale;
+
+  if constexpr (kTranspose) {
+    // O (wide) is cols x rows: stage O rows tc*64.. (= W columns) into smem.
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int idx = threadIdx.x + kThreads * j;
+      const int orow_l = idx >> 3;
+      const int seg = (idx & 7) * 8;
+      const int orow = tc * T + orow_l;
+      const int ocol = tr * T + seg;
+      if (orow < cols) {
+        const uint16_t* src = Om + static_cast<int64_t>(orow) * o_ld + ocol;
+        if (ocol + 7 < rows && ((o_ld & 7) == 0)) {
+          *reinterpret_cast<uint4*>(&sO[orow_l][seg]) = __ldg(reinterpret_cast<const uint4*>(src));
+        } else {
+          for (int e = 0; e < 8; ++e) sO[orow_l][seg + e] = (ocol + e < rows) ? src[e] : 0;
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  const int rr = threadIdx.x >> 4;
+  const int cc = (threadIdx.x & 15) * 4;
+  const bool vec_ok = (cols & 3) == 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int lr_ = rr + 16 * i;
+    const int r = tr * T + lr_;
+    const int c = tc * T + cc;
+    if (r >= rows) continue;
+    float o[4];
+    if constexpr (kTranspose) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = bf16_to_f32(sO[cc + e][lr_]);
+    } else {
+      const uint16_t* src = Om + static_cast<int64_t>(r) * o_ld + c;
+      if (c + 3 < cols && ((o_ld & 3) == 0)) {
+        const uint2 p = __ldg(reinterpret_cast<const uint2*>(src));
+        o[0] = bf16_to_f32(p.x & 0xFFFFu); o[1] = bf16_to_f32(p.x >> 16);
+        o[2] = bf16_to_f32(p.y & 0xFFFFu); o[3] = bf16_to_f32(p.y >> 16);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = (c + e < cols) ? bf16_to_f32(src[e]) : 0.f;
+      }
+    }
+    const int64_t off = static_cast<int64_t>(r) * cols + c;
+    if (vec_ok && c + 3 < cols) {
+      float4 w4 = *reinterpret_cast<const float4*>(Wm + off);
+      w4.x = fmaf(w4.x, decay, -step * o[0]);
+      w4.y = fmaf(w4.y, decay, -step * o[1]);
+      w4.z = fmaf(w4.z, decay, -step * o[2]);
+      w4.w = fmaf(w4.w, decay, -step * o[3]);
+      *reinterpret_cast<float4*>(Wm + off) = w4;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (c + e < cols) Wm[off + e] = fmaf(Wm[off + e], decay, -step * o[e]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) scale_bf16_kernel(
+    int m, int n, const uint16_t* __restrict__ x, int64_t x_ld, int64_t x_ms,
+    uint16_t* __restrict__ out, int64_t o_ld, int64_t o_ms, const float* __restrict__ inv_norm) {
+  const int64_t mat = blockIdx.y;
+  const float s = inv_norm[mat];
+  const int64_t total = static_cast<int64_t>(m) * n;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t r = i / n, c = i % n;
+    const float v = bf16_to_f32(x[mat * x_ms + r * x_ld + c]) * s;
+    out[mat * o_ms + r * o_ld + c] = bf16_bits(v);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_momentum_cast(int rows, int cols, int count, float* M, const float* G,
+                                 float mu, uint16_t* X, int64_t x_ld, int64_t x_ms,
+                                 float* partials, cudaStream_t stream) {
+  if (count <= 0) return cudaSuccess;
+  const dim3 grid(ew_tiles_per_matrix(rows, cols), count);
+  if (rows > cols)
+    momentum_cast_kernel<true><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X, x_ld, x_ms,
+                                                              partials);
+  else
+    momentum_cast_kernel<false><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X, x_ld,
+                                                               x_ms, partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const float* partials, int per_matrix, int count, float eps,
+                                 float* inv_norm, int* err, cudaStream_t stream) {
+  if (count <= 0) return cudaSuccess;
+  norm_finalize_kernel<<<count, kThreads, 0, stream>>>(partials, per_matrix, eps, inv_norm, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply_update(int rows, int cols, int count, float* W, const uint16_t* O,
+                                int64_t o_ld, int64_t o_ms, float lr, float wd, float scale,
+                                cudaStream_t stream) {
+  if (count <= 0) return cudaSuccess;
+  const dim3 grid(ew_tiles_per_matrix(rows, cols), count);
+  if (rows > cols)
+    apply_update_kernel<true><<<grid, kThreads, 0, stream>>>(rows, cols, W, O, o_ld, o_ms, lr, wd,
+                                                             scale);
+  else
+    apply_update_kernel<false><<<grid, kThreads, 0, stream>>>(rows, cols, W, O, o_ld, o_ms, lr,
+                                                              wd, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_bf16(int m, int n, int count, const uint16_t* x, int64_t x_ld,
+                              int64_t x_ms, uint16_t* out, int64_t o_ld, int64_t o_ms,
+                              const float* inv_norm, cudaStream_t stream) {
+  if (count <= 0) return cudaSuccess;
+  const int64_t total = static_cast<int64_t>(m) * n;
+  int64_t blocks = (total + kThreads - 1) / kThreads;
+  if (blocks > 4096) blocks = 4096;
+  const dim3 grid(static_cast<unsigned>(blocks), count);
+  scale_bf16_kernel<<<grid, kThreads, 0, stream>>>(m, n, x, x_ld, x_ms, out, o_ld, o_ms, inv_norm);
+  return cudaGetLastError();
+}
+
+}  // namespace muon

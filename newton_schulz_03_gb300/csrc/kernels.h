@@ -1,0 +1,71 @@
+// kernels.h -- internal launch interface between the host library
+// (muon_api.cpp) and the CUDA translation units.  Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace muon {
+
+// Device error bits written by kernels into the handle's flag word.
+constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrNonFinite = 2;
+
+// Elementwise kernels work on 64 x 64 tiles of the source matrix.
+constexpr int kEwTile = 64;
+
+inline int ew_tiles_per_matrix(int rows, int cols) {
+  return ((rows + kEwTile - 1) / kEwTile) * ((cols + kEwTile - 1) / kEwTile);
+}
+
+// Step 1: M <- mu*M + G (FP32, in place); X <- bf16_rne(M) in wide layout
+// (transposed when rows > cols) with row pitch x_ld and matrix pitch x_ms
+// (elements); partials[mat * tiles + tile] <- sum of M^2 over the tile.
+cudaError_t launch_momentum_cast(int rows, int cols, int count, float* M, const float* G,
+                                 float mu, uint16_t* X, int64_t x_ld, int64_t x_ms,
+                                 float* partials, cudaStream_t stream);
+
+// inv_norm[mat] <- 1 / (sqrt(sum of partials of mat) + eps); flags NaN/Inf.
+cudaError_t launch_norm_finalize(const float* partials, int per_matrix, int count, float eps,
+                                 float* inv_norm, int* err, cudaStream_t stream);
+
+// Step 5: W <- W (1 - lr wd) - lr scale O, O in wide layout (pitches in
+// elements), transposed back when rows > cols.
+cudaError_t launch_apply_update(int rows, int cols, int count, float* W, const uint16_t* O,
+                                int64_t o_ld, int64_t o_ms, float lr, float wd, float scale,
+                                cudaStream_t stream);
+
+// ns_steps == 0: out <- bf16(inv_norm[mat] * x), both m x n with pitches.
+cudaError_t launch_scale_bf16(int m, int n, int count, const uint16_t* x, int64_t x_ld,
+                              int64_t x_ms, uint16_t* out, int64_t o_ld, int64_t o_ms,
+                              const float* inv_norm, cudaStream_t stream);
+
+// ------------------------------------------------------------------ NS GEMMs
+// A BF16 matrix batch: element pointer, row pitch and matrix pitch (elements).
+struct BatchView {
+  const void* ptr;
+  int64_t ld;
+  int64_t ms;
+};
+
+// Set up kernel attributes once per process (dynamic shared memory).
+cudaError_t ns_gemm_init();
+
+// A = alpha * X X^T, alpha = inv_norm[mat]^2 (or 1 when inv_norm == NULL).
+// X: m x n, A: m x m.  Upper-triangle tiles only, mirrored.
+cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out,
+                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream);
+
+// B = b A + c A A (A symmetric m x m).  Upper-triangle tiles only, mirrored.
+cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float b, float c,
+                           int* err, int grid_cap, cudaStream_t stream);
+
+// X' = alpha (a X + B X), alpha = inv_norm[mat] (or 1 when NULL).
+cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X,
+                             BatchView X_out, float a, const float* inv_norm, int* err,
+                             int grid_cap, cudaStream_t stream);
+
+// Last error text of a tensor-map encode (host, thread-local).
+const char* ns_last_encode_error();
+
+}  // namespace muon

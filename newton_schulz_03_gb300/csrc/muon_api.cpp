@@ -1,0 +1,765 @@
+// muon_api.cpp -- host side of the C ABI declared in include/muon.h.
+//
+// Responsibilities: argument validation (nothing is launched for an invalid
+// call), the shape-group planner ("parameters of identical shape are packed
+// into one batch", Frontier Pre-training at Microsoft AI, Method details §5,
+// resharding step 2), the device workspace, the launch sequence of one step,
+// per-kernel event timing and the device error flag.
+//
+// Plan: caller groups are keyed by their wide shape (m, n) = (min, max), so a
+// tall group joins the batch of its transpose.  A batch is cut into chunks
+// that fit the workspace.  Per chunk: momentum_cast for each caller segment,
+// one norm finalisation, ns_steps x (gram, poly, update), apply for each
+// segment.  The plan of a group list is cached, as the pages cache their
+// resharding metadata ("resharding metadata caching").
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/muon.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+muon_status_t fail(muon_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+muon_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(MUON_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kDefaultWorkspace = size_t(8) << 30;  // 8 GiB
+constexpr size_t kAlign = 256;
+constexpr int kMaxDim = 1 << 20;
+constexpr int kMaxSteps = 64;
+constexpr int64_t kMaxMatrixElems = int64_t(1) << 34;
+
+// Largest matrix count per launch so that tile indices fit in int32 (the
+// update product has the most tiles: ceil(m/128) * ceil(n/256); the Gram
+// product has t(t+1)/2 with t = ceil(m/128)).
+int64_t max_count_per_launch(int m, int n) {
+  const int64_t tm = (m + 127) / 128, tn = (n + 255) / 256;
+  const int64_t per = std::max(tm * tn, tm * (tm + 1) / 2);
+  return std::max<int64_t>(1, (int64_t(1) << 30) / per);
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
+
+// Workspace layout of one chunk of `cap` matrices of wide shape m x n.
+struct ChunkLayout {
+  int64_t ldx, ldm;  // row pitches (elements) of X and of A/B
+  int tiles;         // elementwise tiles per matrix (norm partials)
+  size_t off_x0, off_x1, off_a, off_b, off_part, off_inv, bytes;
+};
+
+ChunkLayout chunk_layout(int m, int n, int64_t cap) {
+  ChunkLayout L{};
+  L.ldx = pad8(n);
+  L.ldm = pad8(m);
+  L.tiles = muon::ew_tiles_per_matrix(m, n);
+  size_t off = 0;
+  const size_t xb = align_up(size_t(cap) * m * L.ldx * 2, kAlign);
+  const size_t ab = align_up(size_t(cap) * m * L.ldm * 2, kAlign);
+  L.off_x0 = off; off += xb;
+  L.off_x1 = off; off += xb;
+  L.off_a = off; off += ab;
+  L.off_b = off; off += ab;
+  L.off_part = off; off += align_up(size_t(cap) * L.tiles * 4, kAlign);
+  L.off_inv = off; off += align_up(size_t(cap) * 4, kAlign);
+  L.bytes = off;
+  return L;
+}
+
+size_t per_matrix_bytes(int m, int n) {
+  const int64_t ldx = pad8(n), ldm = pad8(m);
+  return size_t(2) * m * ldx * 2 + size_t(2) * m * ldm * 2 +
+         size_t(muon::ew_tiles_per_matrix(m, n)) * 4 + 4;
+}
+
+struct Segment {
+  int group;        // caller group index
+  int64_t first;    // first matrix of the group in this segment
+  int count;        // matrices
+  int slot;         // first slot in the chunk
+};
+
+struct Chunk {
+  int m, n;
+  int count;
+  std::vector<Segment> segs;
+};
+
+struct Plan {
+  std::vector<Chunk> chunks;
+  int n_batches = 0;
+  int max_chunk = 0;
+  int64_t matrices = 0;
+  size_t ws_bytes = 0;
+  double flops = 0.0;
+  int64_t launches = 0;
+};
+
+muon_status_t validate_groups(const muon_group_t* groups, int32_t n_groups) {
+  if (n_groups < 0) return fail(MUON_ERR_INVALID_ARG, "n_groups < 0");
+  if (n_groups > 0 && groups == nullptr) return fail(MUON_ERR_INVALID_ARG, "groups is NULL");
+  for (int g = 0; g < n_groups; ++g) {
+    const muon_group_t& G = groups[g];
+    if (G.rows < 1 || G.cols < 1 || G.rows > kMaxDim || G.cols > kMaxDim)
+      return fail(MUON_ERR_INVALID_ARG, "group %d: rows/cols out of range (%d x %d)", g, G.rows,
+                  G.cols);
+    if (G.count < 0) return fail(MUON_ERR_INVALID_ARG, "group %d: count < 0", g);
+    if (int64_t(G.rows) * G.cols > kMaxMatrixElems)
+      return fail(MUON_ERR_INVALID_ARG, "group %d: matrix of %d x %d is too large", g, G.rows,
+                  G.cols);
+    if (!std::isfinite(G.update_scale))
+      return fail(MUON_ERR_INVALID_ARG, "group %d: update_scale not finite", g);
+  }
+  return MUON_OK;
+}
+
+muon_status_t build_plan(const muon_group_t* groups, int32_t n_groups, int32_t ns_steps,
+                         size_t ws_cap, Plan* plan) {
+  muon_status_t st = validate_groups(groups, n_groups);
+  if (st != MUON_OK) return st;
+  if (ns_steps < 0 || ns_steps > kMaxSteps)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps out of range (%d)", ns_steps);
+  if (ws_cap == 0) ws_cap = kDefaultWorkspace;
+  // Batches keyed by wide shape, in order of first appearance.
+  std::vector<std::pair<std::pair<int, int>, std::vector<int>>> batches;
+  std::map<std::pair<int, int>, size_t> index;
+  for (int g = 0; g < n_groups; ++g) {
+    if (groups[g].count == 0) continue;
+    const std::pair<int, int> key{std::min(groups[g].rows, groups[g].cols),
+                                  std::max(groups[g].rows, groups[g].cols)};
+    auto it = index.find(key);
+    if (it == index.end()) {
+      index[key] = batches.size();
+      batches.push_back({key, {g}});
+    } else {
+      batches[it->second].second.push_back(g);
+    }
+  }
+  Plan P;
+  P.n_batches = static_cast<int>(batches.size());
+  for (auto& b : batches) {
+    const int m = b.first.first, n = b.first.second;
+    int64_t total = 0;
+    for (int g : b.second) total += groups[g].count;
+    const size_t pm = per_matrix_bytes(m, n);
+    int64_t cap = static_cast<int64_t>((ws_cap > 8 * kAlign ? ws_cap - 8 * kAlign : 0) / pm);
+    if (cap < 1) cap = 1;  // a single matrix always gets room
+    if (cap > total) cap = total;
+    if (cap > 65535) cap = 65535;  // grid.y limit of the elementwise kernels
+    cap = std::min(cap, max_count_per_launch(m, n));
+    P.ws_bytes = std::max(P.ws_bytes, chunk_layout(m, n, cap).bytes);
+    P.matrices += total;
+    P.flops += double(total) * ns_steps * (3.0 * m * double(m) * n + double(m) * m * m);
+    // Cut the batch into chunks of at most `cap` matrices.
+    Chunk cur{m, n, 0, {}};
+    for (int g : b.second) {
+      int64_t done = 0;
+      while (done < groups[g].count) {
+        const int64_t take = std::min<int64_t>(groups[g].count - done, cap - cur.count);
+        cur.segs.push_back({g, done, static_cast<int>(take), cur.count});
+        cur.count += static_cast<int>(take);
+        done += take;
+        if (cur.count == cap) {
+          P.chunks.push_back(cur);
+          cur = Chunk{m, n, 0, {}};
+        }
+      }
+    }
+    if (cur.count > 0) P.chunks.push_back(cur);
+  }
+  for (const Chunk& c : P.chunks) {
+    P.max_chunk = std::max(P.max_chunk, c.count);
+    P.launches += 2 * static_cast<int64_t>(c.segs.size()) + 1 + (ns_steps > 0 ? 3 * ns_steps : 1);
+  }
+  *plan = std::move(P);
+  return MUON_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// ---------------------------------------------------------------- the handle
+struct muon_handle_s {
+  int device = 0;
+  int num_sms = 0;
+  size_t ws_cap = kDefaultWorkspace;
+  void* ws = nullptr;
+  size_t ws_size = 0;
+  int* dev_err = nullptr;
+  float* staging = nullptr;
+  size_t staging_bytes = 0;
+  // ns entry point scratch: one extra X buffer plus A and B
+  // (lives in the workspace).
+  bool timing = false;
+  struct Pending {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> free_events;
+  muon_kernel_stats_t stats{};
+  // Plan cache keyed by the group list and step count.
+  std::string plan_key;
+  Plan plan;
+};
+
+namespace {
+
+cudaEvent_t get_event(muon_handle_t h) {
+  if (!h->free_events.empty()) {
+    cudaEvent_t e = h->free_events.back();
+    h->free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one kernel launch for accounting and (optionally) timing.
+struct LaunchScope {
+  muon_handle_t h;
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  LaunchScope(muon_handle_t h_, int kind_, cudaStream_t s_) : h(h_), kind(kind_), s(s_) {
+    if (h->timing) {
+      a = get_event(h);
+      cudaEventRecord(a, s);
+    }
+  }
+  ~LaunchScope() {
+    h->stats.launches[kind] += 1;
+    h->stats.total_launches += 1;
+    if (h->timing && a != nullptr) {
+      cudaEvent_t b = get_event(h);
+      cudaEventRecord(b, s);
+      h->pending.push_back({kind, a, b});
+    }
+  }
+};
+
+muon_status_t ensure_workspace(muon_handle_t h, size_t bytes) {
+  if (h->ws_size >= bytes) return MUON_OK;
+  if (h->ws != nullptr) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    cudaFree(h->ws);
+    h->ws = nullptr;
+    h->ws_size = 0;
+  }
+  cudaError_t e = cudaMalloc(&h->ws, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MUON_ERR_NOMEM, "workspace allocation of %zu bytes failed: %s", bytes,
+                cudaGetErrorString(e));
+  }
+  h->ws_size = bytes;
+  return MUON_OK;
+}
+
+struct Coeffs {
+  float a, b, c;
+};
+
+// ns_steps iterations on `count` wide matrices.  Reads x (never written);
+// iteration k writes dst[k]; the last one lands in `out`.  A, B: scratch.
+muon_status_t run_newton_schulz(muon_handle_t h, int m, int n, int count, muon::BatchView x,
+                                muon::BatchView out, muon::BatchView other, muon::BatchView A,
+                                muon::BatchView B, const float* inv_norm, int steps, Coeffs co,
+                                cudaStream_t s) {
+  if (steps == 0) {
+    LaunchScope L(h, MUON_KERNEL_SCALE, s);
+    cudaError_t e = muon::launch_scale_bf16(
+        m, n, count, static_cast<const uint16_t*>(x.ptr), x.ld, x.ms,
+        static_cast<uint16_t*>(const_cast<void*>(out.ptr)), out.ld, out.ms, inv_norm, s);
+    if (e != cudaSuccess) return cuda_fail(e, "scale kernel launch");
+    return MUON_OK;
+  }
+  muon::BatchView src = x;
+  for (int k = 0; k < steps; ++k) {
+    // Alternate so that the final iteration writes `out`.
+    const bool to_out = ((steps - 1 - k) % 2) == 0;
+    muon::BatchView dst = to_out ? out : other;
+    const float* inv = (k == 0) ? inv_norm : nullptr;
+    cudaError_t e;
+    {
+      LaunchScope L(h, MUON_KERNEL_NS_GRAM, s);
+      e = muon::ns_launch_gram(m, n, count, src, A, inv, h->dev_err, h->num_sms, s);
+    }
+    if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "gram launch: %s %s", cudaGetErrorString(e),
+                                      muon::ns_last_encode_error());
+    {
+      LaunchScope L(h, MUON_KERNEL_NS_POLY, s);
+      e = muon::ns_launch_poly(m, count, A, B, co.b, co.c, h->dev_err, h->num_sms, s);
+    }
+    if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "poly launch: %s %s", cudaGetErrorString(e),
+                                      muon::ns_last_encode_error());
+    {
+      LaunchScope L(h, MUON_KERNEL_NS_UPDATE, s);
+      e = muon::ns_launch_update(m, n, count, B, src, dst, co.a, inv, h->dev_err, h->num_sms, s);
+    }
+    if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "update launch: %s %s",
+                                      cudaGetErrorString(e), muon::ns_last_encode_error());
+    src = dst;
+  }
+  return MUON_OK;
+}
+
+std::string plan_key_of(const muon_group_t* groups, int32_t n, int32_t steps) {
+  std::string k;
+  k.reserve(16 * n + 8);
+  char buf[64];
+  snprintf(buf, sizeof(buf), "%d;", steps);
+  k += buf;
+  for (int i = 0; i < n; ++i) {
+    snprintf(buf, sizeof(buf), "%d,%d,%d;", groups[i].rows, groups[i].cols, groups[i].count);
+    k += buf;
+  }
+  return k;
+}
+
+muon_status_t check_handle(muon_handle_t h) {
+  if (h == nullptr) return fail(MUON_ERR_INVALID_ARG, "handle is NULL");
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != h->device) {
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  }
+  return MUON_OK;
+}
+
+bool finite3(float a, float b, float c) {
+  return std::isfinite(a) && std::isfinite(b) && std::isfinite(c);
+}
+
+}  // namespace
+
+// ======================================================================== ABI
+extern "C" {
+
+const char* muon_status_string(muon_status_t s) {
+  switch (s) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG";
+    case MUON_ERR_NOMEM: return "MUON_ERR_NOMEM";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
+    case MUON_ERR_UNSUPPORTED_ARCH: return "MUON_ERR_UNSUPPORTED_ARCH";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+    case MUON_ERR_NONFINITE: return "MUON_ERR_NONFINITE";
+    case MUON_ERR_NO_DEVICE: return "MUON_ERR_NO_DEVICE";
+  }
+  return "MUON_ERR_UNKNOWN";
+}
+
+const char* muon_last_error_message(void) { return g_last_error.c_str(); }
+
+const char* muon_version(void) { return "muon-gb300 0.1.0 (sm_103a)"; }
+
+muon_status_t muon_create(muon_handle_t* out, int32_t device, size_t workspace_bytes_max) {
+  if (out == nullptr) return fail(MUON_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return fail(MUON_ERR_NO_DEVICE, "no CUDA device visible (%s)",
+                e == cudaSuccess ? "count 0" : cudaGetErrorString(e));
+  }
+  if (device < 0) {
+    e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  }
+  if (device >= ndev) return fail(MUON_ERR_INVALID_ARG, "device %d >= %d devices", device, ndev);
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (major != 10 || minor != 3)
+    return fail(MUON_ERR_UNSUPPORTED_ARCH, "device %d is sm_%d%d; this library is built for sm_103a",
+                device, major, minor);
+  e = cudaSetDevice(device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  e = muon::ns_gemm_init();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel attribute setup");
+  muon_handle_t h = new muon_handle_s();
+  h->device = device;
+  h->num_sms = sms;
+  h->ws_cap = workspace_bytes_max == 0 ? kDefaultWorkspace : workspace_bytes_max;
+  e = cudaMalloc(reinterpret_cast<void**>(&h->dev_err), 256);
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(MUON_ERR_NOMEM, "error-flag allocation failed: %s", cudaGetErrorString(e));
+  }
+  cudaMemset(h->dev_err, 0, 256);
+  cudaDeviceSynchronize();
+  *out = h;
+  return MUON_OK;
+}
+
+muon_status_t muon_destroy(muon_handle_t h) {
+  if (h == nullptr) return MUON_OK;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  for (auto& p : h->pending) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  for (cudaEvent_t e : h->free_events) cudaEventDestroy(e);
+  if (h->ws) cudaFree(h->ws);
+  if (h->staging) cudaFree(h->staging);
+  if (h->dev_err) cudaFree(h->dev_err);
+  delete h;
+  return MUON_OK;
+}
+
+muon_status_t muon_plan_describe(const muon_group_t* groups, int32_t n_groups, int32_t ns_steps,
+                                 size_t workspace_bytes_max, muon_plan_info_t* out) {
+  if (out == nullptr) return fail(MUON_ERR_INVALID_ARG, "out is NULL");
+  Plan P;
+  muon_status_t st = build_plan(groups, n_groups, ns_steps, workspace_bytes_max, &P);
+  if (st != MUON_OK) return st;
+  out->n_batches = P.n_batches;
+  out->n_chunks = static_cast<int32_t>(P.chunks.size());
+  out->max_chunk_matrices = P.max_chunk;
+  out->matrices = P.matrices;
+  out->workspace_bytes = P.ws_bytes;
+  out->ns_algorithmic_flops = P.flops;
+  out->launches_per_step = P.launches;
+  return MUON_OK;
+}
+
+muon_status_t muon_step(muon_handle_t h, const muon_group_t* groups, int32_t n_groups,
+                        float* const* momentum, const float* const* grad, float* const* weights,
+                        float lr, float wd, float mu, int32_t ns_steps, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  if (!finite3(lr, wd, mu)) return fail(MUON_ERR_INVALID_ARG, "lr, wd and mu must be finite");
+  st = validate_groups(groups, n_groups);
+  if (st != MUON_OK) return st;
+  if (n_groups > 0 && (momentum == nullptr || grad == nullptr || weights == nullptr))
+    return fail(MUON_ERR_INVALID_ARG, "pointer arrays must not be NULL");
+  for (int g = 0; g < n_groups; ++g) {
+    if (groups[g].count == 0) continue;
+    if (momentum[g] == nullptr || grad[g] == nullptr || weights[g] == nullptr)
+      return fail(MUON_ERR_INVALID_ARG, "group %d: NULL buffer", g);
+    if (!aligned16(momentum[g]) || !aligned16(grad[g]) || !aligned16(weights[g]))
+      return fail(MUON_ERR_INVALID_ARG, "group %d: buffers must be 16-byte aligned", g);
+  }
+  const std::string key = plan_key_of(groups, n_groups, ns_steps);
+  if (key != h->plan_key) {
+    Plan P;
+    st = build_plan(groups, n_groups, ns_steps, h->ws_cap, &P);
+    if (st != MUON_OK) return st;
+    h->plan = std::move(P);
+    h->plan_key = key;
+  }
+  const Plan& P = h->plan;
+  st = ensure_workspace(h, P.ws_bytes);
+  if (st != MUON_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Coeffs co{MUON_NS_A, MUON_NS_B, MUON_NS_C};
+  uint8_t* ws = static_cast<uint8_t*>(h->ws);
+  for (const Chunk& c : P.chunks) {
+    const ChunkLayout L = chunk_layout(c.m, c.n, c.count);
+    uint16_t* x0 = reinterpret_cast<uint16_t*>(ws + L.off_x0);
+    uint16_t* x1 = reinterpret_cast<uint16_t*>(ws + L.off_x1);
+    uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.off_a);
+    uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.off_b);
+    float* part = reinterpret_cast<float*>(ws + L.off_part);
+    float* inv = reinterpret_cast<float*>(ws + L.off_inv);
+    const int64_t xms = int64_t(c.m) * L.ldx, ams = int64_t(c.m) * L.ldm;
+    for (const Segment& sg : c.segs) {
+      const muon_group_t& G = groups[sg.group];
+      const int64_t off = sg.first * int64_t(G.rows) * G.cols;
+      LaunchScope Ls(h, MUON_KERNEL_MOMENTUM_CAST, s);
+      cudaError_t e = muon::launch_momentum_cast(G.rows, G.cols, sg.count, momentum[sg.group] + off,
+                                                 grad[sg.group] + off, mu, x0 + sg.slot * xms,
+                                                 L.ldx, xms, part + int64_t(sg.slot) * L.tiles, s);
+      if (e != cudaSuccess) return cuda_fail(e, "momentum_cast launch");
+    }
+    {
+      LaunchScope Ls(h, MUON_KERNEL_NORM, s);
+      cudaError_t e = muon::launch_norm_finalize(part, L.tiles, c.count, MUON_NORM_EPS, inv,
+                                                 h->dev_err, s);
+      if (e != cudaSuccess) return cuda_fail(e, "norm launch");
+    }
+    // The iterates alternate between x0 and x1, starting from x0; the
+    // final one lands in x0 for an even (non-zero) step count, else in x1.
+    uint16_t* fin = (ns_steps > 0 && ns_steps % 2 == 0) ? x0 : x1;
+    uint16_t* oth = (fin == x0) ? x1 : x0;
+    const muon::BatchView vx0{x0, L.ldx, xms}, vfin{fin, L.ldx, xms}, voth{oth, L.ldx, xms};
+    const muon::BatchView vA{A, L.ldm, ams}, vB{B, L.ldm, ams};
+    st = run_newton_schulz(h, c.m, c.n, c.count, vx0, vfin, voth, vA, vB, inv, ns_steps, co, s);
+    if (st != MUON_OK) return st;
+    for (const Segment& sg : c.segs) {
+      const muon_group_t& G = groups[sg.group];
+      const int64_t off = sg.first * int64_t(G.rows) * G.cols;
+      LaunchScope Ls(h, MUON_KERNEL_APPLY, s);
+      cudaError_t e = muon::launch_apply_update(G.rows, G.cols, sg.count, weights[sg.group] + off,
+                                                fin + sg.slot * xms, L.ldx, xms, lr, wd,
+                                                G.update_scale, s);
+      if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+    }
+  }
+  return MUON_OK;
+}
+
+muon_status_t muon_step_host(muon_handle_t h, const muon_group_t* groups, int32_t n_groups,
+                             float* const* momentum_host, const float* const* grad_host,
+                             float* const* weights_host, float lr, float wd, float mu,
+                             int32_t ns_steps, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  st = validate_groups(groups, n_groups);
+  if (st != MUON_OK) return st;
+  if (n_groups > 0 && (momentum_host == nullptr || grad_host == nullptr || weights_host == nullptr))
+    return fail(MUON_ERR_INVALID_ARG, "pointer arrays must not be NULL");
+  size_t total = 0;
+  std::vector<size_t> offs(n_groups);
+  for (int g = 0; g < n_groups; ++g) {
+    offs[g] = total;
+    const size_t ne = size_t(groups[g].rows) * groups[g].cols * groups[g].count;
+    if (ne > 0 && (momentum_host[g] == nullptr || grad_host[g] == nullptr ||
+                   weights_host[g] == nullptr))
+      return fail(MUON_ERR_INVALID_ARG, "group %d: NULL host buffer", g);
+    total += align_up(ne, 64);  // 256-byte aligned group slices
+  }
+  const size_t bytes = 3 * total * sizeof(float);
+  if (h->staging_bytes < bytes) {
+    if (h->staging) {
+      cudaDeviceSynchronize();
+      cudaFree(h->staging);
+      h->staging = nullptr;
+      h->staging_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&h->staging), bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(MUON_ERR_NOMEM, "staging allocation of %zu bytes failed", bytes);
+    }
+    h->staging_bytes = bytes;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::vector<float*> dm(n_groups), dw(n_groups);
+  std::vector<const float*> dg(n_groups);
+  for (int g = 0; g < n_groups; ++g) {
+    const size_t ne = size_t(groups[g].rows) * groups[g].cols * groups[g].count;
+    dm[g] = h->staging + offs[g];
+    dg[g] = h->staging + total + offs[g];
+    dw[g] = h->staging + 2 * total + offs[g];
+    if (ne == 0) continue;
+    cudaError_t e = cudaMemcpyAsync(dm[g], momentum_host[g], ne * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<float*>(dg[g]), grad_host[g], ne * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dw[g], weights_host[g], ne * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+  }
+  st = muon_step(h, groups, n_groups, dm.data(), dg.data(), dw.data(), lr, wd, mu, ns_steps, stream);
+  if (st != MUON_OK) return st;
+  for (int g = 0; g < n_groups; ++g) {
+    const size_t ne = size_t(groups[g].rows) * groups[g].cols * groups[g].count;
+    if (ne == 0) continue;
+    cudaError_t e = cudaMemcpyAsync(momentum_host[g], dm[g], ne * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(weights_host[g], dw[g], ne * 4, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+  }
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return MUON_OK;
+}
+
+muon_status_t muon_momentum_cast(muon_handle_t h, int32_t rows, int32_t cols, int32_t count,
+                                 float* momentum, const float* grad, float mu, uint16_t* x_wide,
+                                 float* inv_norm, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  const muon_group_t g{rows, cols, count, 1.0f};
+  st = validate_groups(&g, 1);
+  if (st != MUON_OK) return st;
+  if (!std::isfinite(mu)) return fail(MUON_ERR_INVALID_ARG, "mu must be finite");
+  if (count == 0) return MUON_OK;
+  if (momentum == nullptr || grad == nullptr || x_wide == nullptr || inv_norm == nullptr)
+    return fail(MUON_ERR_INVALID_ARG, "NULL buffer");
+  if (!aligned16(momentum) || !aligned16(grad) || !aligned16(x_wide) || !aligned16(inv_norm))
+    return fail(MUON_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  const int m = std::min(rows, cols), n = std::max(rows, cols);
+  const int tiles = muon::ew_tiles_per_matrix(rows, cols);
+  const size_t need = align_up(size_t(count) * tiles * 4, kAlign);
+  st = ensure_workspace(h, std::max(need, h->ws_size));
+  if (st != MUON_OK) return st;
+  float* part = static_cast<float*>(h->ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int64_t done = 0; done < count;) {
+    const int take = static_cast<int>(std::min<int64_t>(count - done, 65535));
+    const int64_t off = done * int64_t(rows) * cols;
+    {
+      LaunchScope Ls(h, MUON_KERNEL_MOMENTUM_CAST, s);
+      cudaError_t e = muon::launch_momentum_cast(rows, cols, take, momentum + off, grad + off, mu,
+                                                 x_wide + done * int64_t(m) * n, n,
+                                                 int64_t(m) * n, part + done * tiles, s);
+      if (e != cudaSuccess) return cuda_fail(e, "momentum_cast launch");
+    }
+    done += take;
+  }
+  LaunchScope Ls(h, MUON_KERNEL_NORM, s);
+  cudaError_t e = muon::launch_norm_finalize(part, tiles, count, MUON_NORM_EPS, inv_norm,
+                                             h->dev_err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "norm launch");
+  return MUON_OK;
+}
+
+muon_status_t muon_newton_schulz_bf16(muon_handle_t h, int32_t m, int32_t n, int32_t count,
+                                      const uint16_t* x, uint16_t* out, const float* inv_norm,
+                                      int32_t ns_steps, const float* coeffs, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  if (m < 1 || n < 1 || m > n || m > kMaxDim || n > kMaxDim || count < 0)
+    return fail(MUON_ERR_INVALID_ARG, "need 1 <= m <= n <= %d and count >= 0 (got %d x %d, %d)",
+                kMaxDim, m, n, count);
+  if ((m % 8) != 0 || (n % 8) != 0)
+    return fail(MUON_ERR_INVALID_ARG, "m and n must be multiples of 8 (got %d x %d)", m, n);
+  if (ns_steps < 0 || ns_steps > kMaxSteps)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps out of range (%d)", ns_steps);
+  Coeffs co{MUON_NS_A, MUON_NS_B, MUON_NS_C};
+  if (coeffs != nullptr) {
+    co = Coeffs{coeffs[0], coeffs[1], coeffs[2]};
+    if (!finite3(co.a, co.b, co.c)) return fail(MUON_ERR_INVALID_ARG, "coefficients not finite");
+  }
+  if (count == 0) return MUON_OK;
+  if (x == nullptr || out == nullptr || inv_norm == nullptr)
+    return fail(MUON_ERR_INVALID_ARG, "NULL buffer");
+  if (!aligned16(x) || !aligned16(out)) return fail(MUON_ERR_INVALID_ARG, "x/out must be 16-byte aligned");
+  const size_t xbytes = size_t(count) * m * n * 2;
+  const uintptr_t xb = reinterpret_cast<uintptr_t>(x), ob = reinterpret_cast<uintptr_t>(out);
+  if (xb < ob + xbytes && ob < xb + xbytes) return fail(MUON_ERR_INVALID_ARG, "x and out overlap");
+  // Scratch: one more X buffer and A, B -- in chunks that fit the cap.
+  const size_t pm = align_up(size_t(m) * n * 2, 16) + 2 * align_up(size_t(m) * m * 2, 16);
+  int64_t cap = static_cast<int64_t>(h->ws_cap / pm);
+  if (cap < 1) cap = 1;
+  if (cap > count) cap = count;
+  cap = std::min(cap, max_count_per_launch(m, n));
+  const size_t need = align_up(size_t(cap) * m * n * 2, kAlign) + 2 * align_up(size_t(cap) * m * m * 2, kAlign);
+  st = ensure_workspace(h, need);
+  if (st != MUON_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(h->ws);
+  uint16_t* other = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* A = reinterpret_cast<uint16_t*>(ws + align_up(size_t(cap) * m * n * 2, kAlign));
+  uint16_t* B = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(A) +
+                                            align_up(size_t(cap) * m * m * 2, kAlign));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t xms = int64_t(m) * n, ams = int64_t(m) * m;
+  for (int64_t done = 0; done < count; done += cap) {
+    const int take = static_cast<int>(std::min<int64_t>(count - done, cap));
+    const muon::BatchView vx{x + done * xms, n, xms}, vo{out + done * xms, n, xms};
+    const muon::BatchView vt{other, n, xms}, vA{A, m, ams}, vB{B, m, ams};
+    st = run_newton_schulz(h, m, n, take, vx, vo, vt, vA, vB, inv_norm + done, ns_steps, co, s);
+    if (st != MUON_OK) return st;
+  }
+  return MUON_OK;
+}
+
+muon_status_t muon_apply_update(muon_handle_t h, int32_t rows, int32_t cols, int32_t count,
+                                float* weights, const uint16_t* o_wide, float lr, float wd,
+                                float scale, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  const muon_group_t g{rows, cols, count, scale};
+  st = validate_groups(&g, 1);
+  if (st != MUON_OK) return st;
+  if (!finite3(lr, wd, scale)) return fail(MUON_ERR_INVALID_ARG, "lr, wd, scale must be finite");
+  if (count == 0) return MUON_OK;
+  if (weights == nullptr || o_wide == nullptr) return fail(MUON_ERR_INVALID_ARG, "NULL buffer");
+  if (!aligned16(weights) || !aligned16(o_wide))
+    return fail(MUON_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  const int m = std::min(rows, cols), n = std::max(rows, cols);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int64_t done = 0; done < count;) {
+    const int take = static_cast<int>(std::min<int64_t>(count - done, 65535));
+    LaunchScope Ls(h, MUON_KERNEL_APPLY, s);
+    cudaError_t e = muon::launch_apply_update(rows, cols, take, weights + done * int64_t(rows) * cols,
+                                              o_wide + done * int64_t(m) * n, n, int64_t(m) * n,
+                                              lr, wd, scale, s);
+    if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+    done += take;
+  }
+  return MUON_OK;
+}
+
+muon_status_t muon_last_device_error(muon_handle_t h, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int flag = 0;
+  e = cudaMemcpy(&flag, h->dev_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "error flag read");
+  if (flag != 0) {
+    cudaMemset(h->dev_err, 0, sizeof(int));
+    cudaDeviceSynchronize();
+  }
+  if (flag & muon::kDevErrTimeout) return fail(MUON_ERR_TIMEOUT, "a device-side wait expired");
+  if (flag & muon::kDevErrNonFinite) return fail(MUON_ERR_NONFINITE, "non-finite momentum norm");
+  return MUON_OK;
+}
+
+muon_status_t muon_set_kernel_timing(muon_handle_t h, int32_t enable) {
+  if (h == nullptr) return fail(MUON_ERR_INVALID_ARG, "handle is NULL");
+  h->timing = enable != 0;
+  return MUON_OK;
+}
+
+muon_status_t muon_kernel_stats(muon_handle_t h, muon_kernel_stats_t* out) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  if (out == nullptr) return fail(MUON_ERR_INVALID_ARG, "out is NULL");
+  if (!h->pending.empty()) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    for (auto& p : h->pending) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) h->stats.total_ms[p.kind] += ms;
+      h->free_events.push_back(p.a);
+      h->free_events.push_back(p.b);
+    }
+    h->pending.clear();
+  }
+  *out = h->stats;
+  return MUON_OK;
+}
+
+muon_status_t muon_reset_kernel_stats(muon_handle_t h) {
+  muon_kernel_stats_t tmp;
+  muon_status_t st = muon_kernel_stats(h, &tmp);  // drains pending events
+  if (st != MUON_OK) return st;
+  h->stats = muon_kernel_stats_t{};
+  return MUON_OK;
+}
+
+}  // extern "C"

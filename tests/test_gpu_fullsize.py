@@ -1,0 +1,151 @@
+"""Full-size parity: the workloads at their real sizes, in the launch
+configuration the benchmark times (one muon_step over every group of the
+workload), checked on sampled matrices against the CPU oracle.
+
+Matrices the FP64 oracle cannot finish in seconds (8704 x 8704 and
+8704 x 13056) are checked through properties that hold at any size: the
+momentum update and cast element-wise, and for the orthogonalised update
+the symmetry of O X0^T (= q(A) A for the polynomial q of the iteration)
+plus agreement with an FP32 re-statement of the iteration on cuBLAS.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import muon_oracle as o
+from tests.gpu_helpers import ulp_close
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+NS_TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def ns():
+    from newton_schulz_03_gb300 import build_lib
+    build_lib.build()
+    import newton_schulz_03_gb300 as pkg
+    return pkg
+
+
+def free_bytes():
+    free, _ = torch.cuda.mem_get_info()
+    return free
+
+
+def step_workload(ns, wname, samples, heavy=None):
+    """Step a whole workload once on device-generated inputs; return the
+    sampled matrices' inputs and outputs on the host."""
+    from newton_schulz_03_gb300.workloads import WORKLOADS, make_group_torch
+    w = WORKLOADS[wname]
+    need = sum(g.numel for g in w.groups) * 12 + (9 << 30)
+    if free_bytes() < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free on the device")
+    groups = [(g.rows, g.cols, g.count) for g in w.groups]
+    tensors = [make_group_torch(w, gi, "cuda") for gi in range(len(w.groups))]
+    before = {(gi, i): tuple(t[i].cpu().numpy() for t in tensors[gi])
+              for gi, i in samples + (heavy or [])}
+    Ws, Ms, Gs = ([t[k] for t in tensors] for k in range(3))
+    with ns.Handle() as h:
+        ns.muon_step(h.value, groups, Ms, Gs, Ws, w.lr, w.wd, w.mu, w.ns_steps)
+        ns.muon_last_device_error(h.value)
+    after = {(gi, i): (Ws[gi][i].cpu().numpy(), Ms[gi][i].cpu().numpy())
+             for gi, i in samples + (heavy or [])}
+    del tensors, Ws, Ms, Gs
+    torch.cuda.empty_cache()
+    return w, before, after
+
+
+def check_sample(w, before, after, key):
+    gi, i = key
+    W, M, G = before[key]
+    Wg, Mg = after[key]
+    st = o.muon_step_matrix(W, M, G, lr=w.lr, wd=w.wd, mu=w.mu, ns_steps=w.ns_steps)
+    assert ulp_close(Mg, st.M_new).all()
+    on = np.linalg.norm(st.O)
+    dw = np.linalg.norm(Wg.astype(np.float64) - st.W_new.astype(np.float64))
+    fp = 1e-6 * (np.linalg.norm(W) + w.lr * on)
+    if on == 0.0:
+        assert dw <= fp, "zero momentum must only decay the weights"
+        return 0.0
+    err = (dw - fp) / (w.lr * on)
+    assert err <= NS_TOL, f"group {gi} matrix {i}: update error {err:.3e}"
+    return err
+
+
+def check_heavy(w, before, after, key):
+    """Property checks for a matrix too large for the FP64 oracle."""
+    gi, i = key
+    W, M, G = before[key]
+    Wg, Mg = after[key]
+    Mref = o.momentum_update(M, G, w.mu)
+    assert ulp_close(Mg, Mref).all()
+    # Recover the GPU's update O from the weight change (FP32 arithmetic:
+    # W' = W (1 - lr wd) - lr O).
+    lr, wd = np.float32(w.lr), np.float32(w.wd)
+    decay = np.float32(1.0) - lr * wd
+    O_gpu = (W.astype(np.float64) * float(decay) - Wg.astype(np.float64)) / float(lr)
+    Xb = o.bf16_rne(Mg)
+    transposed = Xb.shape[0] > Xb.shape[1]
+    X = Xb.T if transposed else Xb
+    Og = O_gpu.T if transposed else O_gpu
+    s = o.frobenius_scale(Mg)
+    dev_ = torch.device("cuda")
+    torch.backends.cuda.matmul.allow_tf32 = False   # true FP32 products
+    X0 = torch.from_numpy(X / s).to(dev_, torch.float32)
+    Ot = torch.from_numpy(Og).to(dev_, torch.float32)
+    # FP32 re-statement of the iteration on cuBLAS (not the library's kernels).
+    a, b, c = o.NS_COEFFS
+    Xk = X0.clone()
+    for _ in range(w.ns_steps):
+        A = Xk @ Xk.T
+        B = b * A + c * (A @ A)
+        Xk = a * Xk + B @ Xk
+    err = (torch.linalg.norm(Ot - Xk) / torch.linalg.norm(Xk)).item()
+    # O X0^T is a polynomial in A = X0 X0^T, hence symmetric.
+    S = Ot @ X0.T
+    asym = (torch.linalg.norm(S - S.T) / torch.linalg.norm(S)).item()
+    # The weight change carries FP32 rounding of W (1 - lr wd) ~ 6e-8 |W|,
+    # i.e. ~3e-6 |W| / lr relative to O; allow for it.
+    slack = 4e-6 * np.linalg.norm(W) / (w.lr * torch.linalg.norm(Xk).item())
+    assert err <= NS_TOL + slack, f"group {gi}: {err:.3e}"
+    assert asym <= NS_TOL + slack, f"group {gi}: asymmetry {asym:.3e}"
+
+
+def test_fullsize_l24_attention(ns):
+    # 96 x 2048^2: the benchmark's default workload.
+    w, before, after = step_workload(ns, "l24_attention", [(0, 0), (0, 57), (0, 95)])
+    for k in before:
+        check_sample(w, before, after, k)
+
+
+def test_fullsize_l48_experts(ns):
+    # 1024 matrices: up (1536 x 4096) and down (4096 x 1536, transposed);
+    # matrix 7 of each group has zero gradient and momentum.
+    samples = [(0, 0), (0, 7), (1, 7), (1, 300), (0, 511)]
+    w, before, after = step_workload(ns, "l48_experts", samples)
+    for k in samples:
+        check_sample(w, before, after, k)
+
+
+def test_fullsize_l48_model_layer(ns):
+    # One resident layer of the whole-model step: attention, shared expert,
+    # routed experts and the router in one call.
+    samples = [(0, 3), (1, 0), (2, 0), (3, 100), (4, 511), (5, 0)]
+    w, before, after = step_workload(ns, "l48_model", samples)
+    for k in samples:
+        check_sample(w, before, after, k)
+
+
+def test_fullsize_l102_layer(ns):
+    # 226 GB of FP32 state.  Experts against the oracle; the 8704 x 13056
+    # shared expert and the 8704^2 attention through the size-free checks.
+    samples = [(0, 0), (1, 511), (0, 7)]
+    heavy = [(2, 0), (4, 3)]
+    w, before, after = step_workload(ns, "l102_layer", samples, heavy)
+    for k in samples:
+        check_sample(w, before, after, k)
+    for k in heavy:
+        check_heavy(w, before, after, k)
