@@ -58,6 +58,12 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def job_value(world: int, units_per_rank_step: float, steps: int, secs: float) -> float:
+    """Whole-job throughput: every rank processes its own units each step
+    (weak scaling); the job takes as long as the slowest rank."""
+    return world * units_per_rank_step * steps / secs
+
+
 def barrier(world: int) -> None:
     if world > 1:
         import torch.distributed as dist
@@ -241,7 +247,7 @@ def run_ours(args, world, rank, local):
     gpu_launches = int(round((stats["total_launches"] - launches0) * frac_timed))
 
     matrices_per_step = w.matrices
-    value = world * matrices_per_step * args.steps / secs
+    value = job_value(world, matrices_per_step, args.steps, secs)
     ms_per_step = secs * 1e3 / args.steps
     flops_step = plan["ns_algorithmic_flops"] * layers
     tflops = world * flops_step * args.steps / secs / 1e12
