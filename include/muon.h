@@ -194,6 +194,43 @@ muon_status_t muon_apply_update(muon_handle_t handle, int32_t rows, int32_t cols
                                 float* weights_dev, const uint16_t* o_wide_dev,
                                 float lr, float wd, float scale, void* stream);
 
+/* Newton-Schulz without any memory allocation (no handle).
+ *
+ * The pages have no counterpart of this entry point: it exists for callers
+ * that cannot allocate device memory at the time they orthogonalise --
+ * code running inside CUDA graph construction, custom allocators or
+ * runtimes that must not re-enter the CUDA allocator, and deployments
+ * whose device memory is fixed at start-up.  It computes what
+ * muon_newton_schulz_bf16 computes, with the same arguments and layout,
+ * but its scratch (one more m x n iterate plus the m x m matrices A and B
+ * per matrix) lives in a file-scope device array of
+ * MUON_STATIC_SCRATCH_BYTES (64 MiB) that every GPU loading the library
+ * holds until the process exits.  It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *  - Limit: one matrix must fit the array, i.e.
+ *    2*m*n + 4*m*m bytes (each part rounded up to 256) <= 64 MiB - 256;
+ *    larger matrices are rejected with MUON_ERR_INVALID_ARG and a message
+ *    (muon_last_error_message).  Larger counts are processed in passes.
+ *  - First call on a device: resolves the array's device address
+ *    (cudaGetSymbolAddress) and sets kernel attributes, with that device
+ *    current.  Make that first call before any stream capture.
+ *  - Sharing: every call uses the same array and leaves its last contents
+ *    there; nothing in it needs to start at zero (every scratch element is
+ *    written before it is read).  Calls that overlap on the GPU (different
+ *    streams, or different host threads) race on the array: serialise them.
+ *  - error_flag_dev: optional device int that receives the device error
+ *    bits (1 = a bounded wait expired); the caller zeroes it.  With NULL,
+ *    the bits go to a word inside the array (cleared at each call) and are
+ *    not reported.
+ * Errors: INVALID_ARG (shapes as for muon_newton_schulz_bf16, matrix too
+ * large for the array, NULL or unaligned buffers, overlap), CUDA. */
+#define MUON_STATIC_SCRATCH_BYTES (64u << 20)
+muon_status_t muon_newton_schulz_bf16_static(int32_t m, int32_t n, int32_t count,
+                                             const uint16_t* x_dev, uint16_t* out_dev,
+                                             const float* inv_norm_dev, int32_t ns_steps,
+                                             const float* coeffs_host, int32_t* error_flag_dev,
+                                             void* stream);
+
 /* Synchronise `stream`, then read and clear the handle's device error
  * flag: MUON_OK, MUON_ERR_TIMEOUT or MUON_ERR_NONFINITE. */
 muon_status_t muon_last_device_error(muon_handle_t handle, void* stream);

@@ -30,6 +30,7 @@ EXPORTED = (
     "muon_destroy", "muon_plan_describe", "muon_step", "muon_step_host", "muon_momentum_cast",
     "muon_newton_schulz_bf16", "muon_apply_update", "muon_last_device_error",
     "muon_set_kernel_timing", "muon_kernel_stats", "muon_reset_kernel_stats",
+    "muon_newton_schulz_bf16_static",
 )
 
 
@@ -89,6 +90,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                             P(c_f), c_vp]),
         "muon_apply_update": (c_int, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_f, c_f, c_f,
                                       c_vp]),
+        "muon_newton_schulz_bf16_static": (c_int, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32,
+                                                   P(c_f), c_vp, c_vp]),
         "muon_last_device_error": (c_int, [c_vp, c_vp]),
         "muon_set_kernel_timing": (c_int, [c_vp, c_i32]),
         "muon_kernel_stats": (c_int, [c_vp, P(_Stats)]),
@@ -219,6 +222,19 @@ def muon_newton_schulz_bf16(handle: int, m: int, n: int, count: int, x, out, inv
         c = (ctypes.c_float * 3)(*[float(v) for v in coeffs])
     _check(load_library().muon_newton_schulz_bf16(handle, m, n, count, _ptr(x), _ptr(out),
                                                   _ptr(inv_norm), ns_steps, c, _stream(stream)))
+
+
+def muon_newton_schulz_bf16_static(m: int, n: int, count: int, x, out, inv_norm,
+                                   ns_steps: int = 5, coeffs: Optional[Sequence[float]] = None,
+                                   error_flag=None, stream=None) -> None:
+    """Newton-Schulz with no allocation: scratch lives in the library's
+    fixed static device array (for callers that cannot allocate)."""
+    c = None
+    if coeffs is not None:
+        c = (ctypes.c_float * 3)(*[float(v) for v in coeffs])
+    _check(load_library().muon_newton_schulz_bf16_static(m, n, count, _ptr(x), _ptr(out),
+                                                         _ptr(inv_norm), ns_steps, c,
+                                                         _ptr(error_flag), _stream(stream)))
 
 
 def muon_apply_update(handle: int, rows: int, cols: int, count: int, weights, o_wide,

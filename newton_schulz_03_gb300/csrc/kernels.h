@@ -68,4 +68,8 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X,
 // Last error text of a tensor-map encode (host, thread-local).
 const char* ns_last_encode_error();
 
+// Record `msg` as the calling thread's last error text and return `status`
+// (read back through muon_last_error_message).
+int report(int status, const char* msg);
+
 }  // namespace muon

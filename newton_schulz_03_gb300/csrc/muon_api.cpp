@@ -359,6 +359,13 @@ bool finite3(float a, float b, float c) {
 
 }  // namespace
 
+namespace muon {
+int report(int status, const char* msg) {
+  g_last_error = msg;
+  return status;
+}
+}  // namespace muon
+
 // ======================================================================== ABI
 extern "C" {
 
