@@ -37,18 +37,18 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "kernels.h"
+#include "ns_common.cuh"
 #include "sm103_ptx.cuh"
 
 namespace muon {
 namespace {
 
-enum NsMode : int { kGram = 0, kPoly = 1, kUpdate = 2 };
+using namespace nsk;
 
-constexpr int kBM = 128;      // tile rows (MMA M, TMEM lanes)
-constexpr int kBK = 64;       // K per stage: one 128-byte swizzle row of BF16
 constexpr int kThreads = 192; // 6 warps
 constexpr int kEpiWarps = 4;
 
@@ -64,55 +64,6 @@ struct TileCfg {
   static_assert(kTmemCols <= 512, "two accumulators must fit TMEM");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
-
-struct NsArgs {
-  int32_t m, n;               // X is m x n; A, B are m x m
-  int32_t K;                  // reduction length
-  int32_t tiles_m;            // row tiles per matrix
-  int32_t tiles_n;            // column tiles per matrix (UPDATE)
-  int32_t tiles_per_matrix;
-  int32_t total_tiles;
-  int32_t out_cols;           // columns of the output matrix
-  __nv_bfloat16* out;
-  int64_t out_ld, out_ms;
-  const __nv_bfloat16* aux;   // POLY: A; UPDATE: X
-  int64_t aux_ld, aux_ms;
-  const float* inv_norm;      // alpha source (NULL: alpha = 1)
-  float c0, c1;               // POLY: (b, c); UPDATE: (a, unused)
-  int* err;
-};
-
-__device__ __forceinline__ void decode_tile(const NsArgs& p, int mode, int t, int& mat, int& ti,
-                                            int& tj) {
-  mat = t / p.tiles_per_matrix;
-  int l = t - mat * p.tiles_per_matrix;
-  if (mode == kUpdate) {
-    ti = l / p.tiles_n;
-    tj = l - ti * p.tiles_n;
-  } else {
-    // Upper triangle in row-major order: row i holds tiles_m - i tiles.
-    int i = 0;
-    while (l >= p.tiles_m - i) {
-      l -= p.tiles_m - i;
-      ++i;
-    }
-    ti = i;
-    tj = i + l;
-  }
-}
-
-__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint16_t to_bf16_bits(float v) {
-  __nv_bfloat16 b = __float2bfloat16_rn(v);
-  return *reinterpret_cast<uint16_t*>(&b);
-}
 
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -170,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         int mat, ti, tj;
-        decode_tile(p, MODE, t, mat, ti, tj);
+        decode_tile(p, MODE, kBM, BN, t, mat, ti, tj);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -278,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
       int mat, ti, tj;
-      decode_tile(p, MODE, t, mat, ti, tj);
+      decode_tile(p, MODE, kBM, BN, t, mat, ti, tj);
       const bool got = ptx::mbar_wait(&tmem_full[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
@@ -294,84 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float s = p.inv_norm[mat];
         alpha = (MODE == kGram) ? s * s : s;
       }
-      const int grow = ti * kBM + r_tile;
-      const bool row_ok = grow < p.m;
-      __nv_bfloat16* out_m = p.out + static_cast<int64_t>(mat) * p.out_ms;
-      const __nv_bfloat16* aux_m =
-          (MODE == kGram) ? nullptr : p.aux + static_cast<int64_t>(mat) * p.aux_ms;
-      const bool mirror = (MODE != kUpdate) && (ti != tj);
-
-#pragma unroll 1
-      for (int cb = 0; cb < BN / 32; ++cb) {
-        uint32_t v[32];
-        __syncwarp();  // tcgen05.ld is warp-collective: keep the warp converged
-        ptx::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                    static_cast<uint32_t>(acc * BN + cb * 32),
-                                v);
-        ptx::tmem_ld_wait();
-        const int gcol0 = tj * BN + cb * 32;
-        if (row_ok && gcol0 < p.out_cols) {
-          float f[32];
-          const bool full_chunk = gcol0 + 32 <= p.out_cols;
-          if (MODE == kGram) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) f[e] = alpha * __uint_as_float(v[e]);
-          } else {
-            const __nv_bfloat16* ar = aux_m + static_cast<int64_t>(grow) * p.aux_ld + gcol0;
-            float x[32];
-            if (full_chunk) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint4 u = __ldg(reinterpret_cast<const uint4*>(ar) + q);
-                x[q * 8 + 0] = bf16lo(u.x); x[q * 8 + 1] = bf16hi(u.x);
-                x[q * 8 + 2] = bf16lo(u.y); x[q * 8 + 3] = bf16hi(u.y);
-                x[q * 8 + 4] = bf16lo(u.z); x[q * 8 + 5] = bf16hi(u.z);
-                x[q * 8 + 6] = bf16lo(u.w); x[q * 8 + 7] = bf16hi(u.w);
-              }
-            } else {
-              const uint16_t* a16 = reinterpret_cast<const uint16_t*>(ar);
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                x[e] = (gcol0 + e < p.out_cols) ? __uint_as_float(static_cast<uint32_t>(a16[e]) << 16)
-                                                : 0.f;
-            }
-            if (MODE == kPoly) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) f[e] = fmaf(p.c1, __uint_as_float(v[e]), p.c0 * x[e]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) f[e] = alpha * fmaf(p.c0, x[e], __uint_as_float(v[e]));
-            }
-          }
-          __nv_bfloat16* orow = out_m + static_cast<int64_t>(grow) * p.out_ld + gcol0;
-          if (full_chunk) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 u;
-              u.x = pack_bf16(f[q * 8 + 0], f[q * 8 + 1]);
-              u.y = pack_bf16(f[q * 8 + 2], f[q * 8 + 3]);
-              u.z = pack_bf16(f[q * 8 + 4], f[q * 8 + 5]);
-              u.w = pack_bf16(f[q * 8 + 6], f[q * 8 + 7]);
-              reinterpret_cast<uint4*>(orow)[q] = u;
-            }
-          } else {
-            uint16_t* o16 = reinterpret_cast<uint16_t*>(orow);
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (gcol0 + e < p.out_cols) o16[e] = to_bf16_bits(f[e]);
-          }
-          if (mirror) {
-            // Element (grow, gcol) of an upper off-diagonal tile is also
-            // element (gcol, grow) of the symmetric result.
-            uint16_t* o16 = reinterpret_cast<uint16_t*>(out_m);
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (gcol0 + e < p.out_cols)
-                o16[static_cast<int64_t>(gcol0 + e) * p.out_ld + grow] = to_bf16_bits(f[e]);
-          }
-        }
-      }
-      __syncwarp();
+      epilogue_tile<MODE, BN>(
+          p, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN),
+          mat, ti * kBM + r_tile, ti, tj * BN, alpha);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tmem_empty[acc]);
       acc ^= 1;
@@ -454,15 +330,35 @@ cudaError_t set_attr() {
                               TileCfg<BN>::kSmemBytes);
 }
 
-constexpr int kSymBN = 128;   // symmetric products: square 128 x 128 tiles
+constexpr int kSymBN = 256;   // symmetric products: 128 x 256 tiles (triangular list)
 constexpr int kUpdBN = 256;   // update product: 128 x 256 tiles
+
+int sym_tiles_per_matrix(int tiles_m, int tiles_n) {
+  const int ratio = kSymBN / kBM;
+  int total = 0;
+  for (int i = 0; i < tiles_m; ++i) total += tiles_n - i / ratio;
+  return total;
+}
 
 }  // namespace
 
 const char* ns_last_encode_error() { return g_encode_err; }
 
+// Matrices with more than 128 rows (after the transpose to wide) run on CTA
+// pairs; MUON_NS_PAIR=0 in the environment keeps every product on single
+// CTAs (for comparisons).
+bool use_pairs(int m) {
+  static int enabled = -1;
+  if (enabled < 0) {
+    const char* v = getenv("MUON_NS_PAIR");
+    enabled = (v != nullptr && v[0] == '0') ? 0 : 1;
+  }
+  return enabled == 1 && m > kBM;
+}
+
 cudaError_t ns_gemm_init() {
   cudaError_t e;
+  if ((e = ns_pair_init()) != cudaSuccess) return e;
   if ((e = set_attr<kGram, kSymBN>()) != cudaSuccess) return e;
   if ((e = set_attr<kPoly, kSymBN>()) != cudaSuccess) return e;
   if ((e = set_attr<kUpdate, kUpdBN>()) != cudaSuccess) return e;
@@ -471,16 +367,24 @@ cudaError_t ns_gemm_init() {
 
 cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out,
                            const float* inv_norm, int* err, int grid_cap, cudaStream_t stream) {
-  CUtensorMap tx;
+  if (use_pairs(m)) {
+    CUtensorMap t128;
+    cudaError_t e = make_map(&t128, X, n, m, count, kBM);
+    if (e != cudaSuccess) return e;
+    return ns_pair_gram(t128, m, n, count, A_out, inv_norm, err, grid_cap, stream);
+  }
+  // A-side rows in boxes of kBM, B-side rows in boxes of kSymBN.
+  CUtensorMap tx, txb;
   cudaError_t e = make_map(&tx, X, n, m, count, kBM);
+  if (e == cudaSuccess) e = make_map(&txb, X, n, m, count, kSymBN);
   if (e != cudaSuccess) return e;
   NsArgs p{};
   p.m = m;
   p.n = n;
   p.K = n;
   p.tiles_m = (m + kBM - 1) / kBM;
-  p.tiles_n = p.tiles_m;
-  p.tiles_per_matrix = p.tiles_m * (p.tiles_m + 1) / 2;
+  p.tiles_n = (m + kSymBN - 1) / kSymBN;
+  p.tiles_per_matrix = sym_tiles_per_matrix(p.tiles_m, p.tiles_n);
   p.total_tiles = p.tiles_per_matrix * count;
   p.out_cols = m;
   p.out = static_cast<__nv_bfloat16*>(const_cast<void*>(A_out.ptr));
@@ -489,21 +393,28 @@ cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out
   p.aux = nullptr;
   p.inv_norm = inv_norm;
   p.err = err;
-  return launch<kGram, kSymBN>(tx, tx, p, grid_cap, stream);
+  return launch<kGram, kSymBN>(tx, txb, p, grid_cap, stream);
 }
 
 cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float b, float c,
                            int* err, int grid_cap, cudaStream_t stream) {
-  CUtensorMap ta;
+  if (use_pairs(m)) {
+    CUtensorMap t128;
+    cudaError_t e = make_map(&t128, A, m, m, count, kBM);
+    if (e != cudaSuccess) return e;
+    return ns_pair_poly(t128, m, count, A, B_out, b, c, err, grid_cap, stream);
+  }
+  CUtensorMap ta, tab;
   cudaError_t e = make_map(&ta, A, m, m, count, kBM);
+  if (e == cudaSuccess) e = make_map(&tab, A, m, m, count, kSymBN);
   if (e != cudaSuccess) return e;
   NsArgs p{};
   p.m = m;
   p.n = m;
   p.K = m;
   p.tiles_m = (m + kBM - 1) / kBM;
-  p.tiles_n = p.tiles_m;
-  p.tiles_per_matrix = p.tiles_m * (p.tiles_m + 1) / 2;
+  p.tiles_n = (m + kSymBN - 1) / kSymBN;
+  p.tiles_per_matrix = sym_tiles_per_matrix(p.tiles_m, p.tiles_n);
   p.total_tiles = p.tiles_per_matrix * count;
   p.out_cols = m;
   p.out = static_cast<__nv_bfloat16*>(const_cast<void*>(B_out.ptr));
@@ -516,7 +427,7 @@ cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float
   p.c0 = b;
   p.c1 = c;
   p.err = err;
-  return launch<kPoly, kSymBN>(ta, ta, p, grid_cap, stream);
+  return launch<kPoly, kSymBN>(ta, tab, p, grid_cap, stream);
 }
 
 cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, BatchView X_out,
@@ -528,6 +439,7 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, 
   // X as the MN-major operand: boxes of 64 columns x 64 K-rows.
   e = make_map(&tx, X, n, m, count, kBK);
   if (e != cudaSuccess) return e;
+  if (use_pairs(m)) return ns_pair_update(tb, tx, m, n, count, X, X_out, a, inv_norm, err, grid_cap, stream);
   NsArgs p{};
   p.m = m;
   p.n = n;

@@ -68,6 +68,20 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X,
 // Last error text of a tensor-map encode (host, thread-local).
 const char* ns_last_encode_error();
 
+// CTA-pair (cta_group::2) variants of the three products, 256 x 256 tiles;
+// the tensor maps are built by the ns_launch_* functions above.
+}  // namespace muon
+#include <cuda.h>
+namespace muon {
+cudaError_t ns_pair_init();
+cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchView A_out,
+                         const float* inv_norm, int* err, int grid_cap, cudaStream_t stream);
+cudaError_t ns_pair_poly(const CUtensorMap& ta, int m, int count, BatchView A, BatchView B_out,
+                         float b, float c, int* err, int grid_cap, cudaStream_t stream);
+cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tx, int m, int n, int count,
+                           BatchView X, BatchView X_out, float a, const float* inv_norm, int* err,
+                           int grid_cap, cudaStream_t stream);
+
 // Record `msg` as the calling thread's last error text and return `status`
 // (read back through muon_last_error_message).
 int report(int status, const char* msg);

@@ -1,0 +1,179 @@
+// ns_common.cuh -- pieces shared by the Newton-Schulz product kernels:
+// argument block, tile decoding, and the fused epilogue (TMEM -> registers
+// -> polynomial combine -> BF16 -> global, with mirrored stores for the
+// symmetric products).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace muon {
+namespace nsk {
+
+enum NsMode : int { kGram = 0, kPoly = 1, kUpdate = 2 };
+
+constexpr int kBM = 128;   // accumulator rows per CTA (TMEM lanes)
+constexpr int kBK = 64;    // K per pipeline stage: one 128-byte swizzle row of BF16
+
+struct NsArgs {
+  int32_t m, n;               // X is m x n; A, B are m x m
+  int32_t K;                  // reduction length
+  int32_t tiles_m;            // row tiles per matrix (tile rows = rows per tile)
+  int32_t tiles_n;            // column tiles per matrix
+  int32_t tiles_per_matrix;
+  int32_t total_tiles;
+  int32_t out_cols;           // columns of the output matrix
+  __nv_bfloat16* out;
+  int64_t out_ld, out_ms;
+  const __nv_bfloat16* aux;   // POLY: A; UPDATE: X
+  int64_t aux_ld, aux_ms;
+  const float* inv_norm;      // alpha source (NULL: alpha = 1)
+  float c0, c1;               // POLY: (b, c); UPDATE: (a, unused)
+  int* err;
+};
+
+// Tile t -> (matrix, row tile, column tile).  Symmetric products list, per
+// row tile i, the column tiles j >= floor(i * tile_rows / tile_cols) (the
+// first holds the diagonal); the update product lists every tile.
+__device__ __forceinline__ void decode_tile(const NsArgs& p, int mode, int tile_rows,
+                                            int tile_cols, int t, int& mat, int& ti, int& tj) {
+  mat = t / p.tiles_per_matrix;
+  int l = t - mat * p.tiles_per_matrix;
+  if (mode == kUpdate) {
+    ti = l / p.tiles_n;
+    tj = l - ti * p.tiles_n;
+  } else {
+    int i = 0;
+    while (l >= p.tiles_n - (i * tile_rows) / tile_cols) {
+      l -= p.tiles_n - (i * tile_rows) / tile_cols;
+      ++i;
+    }
+    ti = i;
+    tj = (i * tile_rows) / tile_cols + l;
+  }
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// Epilogue of one accumulator: this thread owns output row `grow` and the
+// BN columns col0 .. col0+BN-1, read from TMEM at `taddr` (lane and column
+// already set).  `rb` is the kBM-row block index of the row (symmetric
+// products: a 128-column sub-block left of it is skipped, right of it is
+// also stored mirrored).  The auxiliary operand (A for POLY, X for UPDATE)
+// is prefetched two 32-column chunks ahead.
+template <int MODE, int BN>
+__device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, int mat, int grow,
+                                              int rb, int col0, float alpha) {
+  constexpr int kChunks = BN / 32;
+  const bool row_ok = grow < p.m;
+  __nv_bfloat16* out_m = p.out + static_cast<int64_t>(mat) * p.out_ms;
+  const __nv_bfloat16* aux_row =
+      (MODE == kGram) ? nullptr
+                      : p.aux + static_cast<int64_t>(mat) * p.aux_ms + static_cast<int64_t>(grow) * p.aux_ld;
+
+  auto chunk_live = [&](int cb) {
+    const int g0 = col0 + cb * 32;
+    const bool below = (MODE != kUpdate) && (g0 / kBM < rb);
+    return row_ok && g0 < p.out_cols && !below;
+  };
+  auto chunk_full = [&](int cb) { return col0 + cb * 32 + 32 <= p.out_cols; };
+
+  uint4 pre[2][4];
+  auto prefetch = [&](int cb, uint4 (&dst)[4]) {
+    if (MODE != kGram && cb < kChunks && chunk_live(cb) && chunk_full(cb)) {
+      const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0 + cb * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = __ldg(src + q);
+    }
+  };
+  prefetch(0, pre[0]);
+  prefetch(1, pre[1]);
+
+#pragma unroll
+  for (int cb = 0; cb < kChunks; ++cb) {
+    uint32_t v[32];
+    __syncwarp();  // tcgen05.ld is warp-collective: keep the warp converged
+    ptx::tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cb * 32), v);
+    ptx::tmem_ld_wait();
+    const int gcol0 = col0 + cb * 32;
+    if (chunk_live(cb)) {
+      const bool full_chunk = chunk_full(cb);
+      const bool mirror = (MODE != kUpdate) && (gcol0 / kBM > rb);
+      float f[32];
+      if (MODE == kGram) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = alpha * __uint_as_float(v[e]);
+      } else {
+        float x[32];
+        if (full_chunk) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 u = pre[cb & 1][q];
+            x[q * 8 + 0] = bf16lo(u.x); x[q * 8 + 1] = bf16hi(u.x);
+            x[q * 8 + 2] = bf16lo(u.y); x[q * 8 + 3] = bf16hi(u.y);
+            x[q * 8 + 4] = bf16lo(u.z); x[q * 8 + 5] = bf16hi(u.z);
+            x[q * 8 + 6] = bf16lo(u.w); x[q * 8 + 7] = bf16hi(u.w);
+          }
+        } else {
+          const uint16_t* a16 = reinterpret_cast<const uint16_t*>(aux_row + gcol0);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            x[e] = (gcol0 + e < p.out_cols) ? __uint_as_float(static_cast<uint32_t>(a16[e]) << 16)
+                                            : 0.f;
+        }
+        if (MODE == kPoly) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) f[e] = fmaf(p.c1, __uint_as_float(v[e]), p.c0 * x[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) f[e] = alpha * fmaf(p.c0, x[e], __uint_as_float(v[e]));
+        }
+      }
+      __nv_bfloat16* orow = out_m + static_cast<int64_t>(grow) * p.out_ld + gcol0;
+      if (full_chunk) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          u.x = pack_bf16(f[q * 8 + 0], f[q * 8 + 1]);
+          u.y = pack_bf16(f[q * 8 + 2], f[q * 8 + 3]);
+          u.z = pack_bf16(f[q * 8 + 4], f[q * 8 + 5]);
+          u.w = pack_bf16(f[q * 8 + 6], f[q * 8 + 7]);
+          reinterpret_cast<uint4*>(orow)[q] = u;
+        }
+      } else {
+        uint16_t* o16 = reinterpret_cast<uint16_t*>(orow);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (gcol0 + e < p.out_cols) o16[e] = to_bf16_bits(f[e]);
+      }
+      if (mirror) {
+        // Element (grow, gcol) above the diagonal is also element (gcol, grow).
+        uint16_t* o16 = reinterpret_cast<uint16_t*>(out_m);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (gcol0 + e < p.out_cols)
+            o16[static_cast<int64_t>(gcol0 + e) * p.out_ld + grow] = to_bf16_bits(f[e]);
+      }
+    }
+    prefetch(cb + 2, pre[cb & 1]);
+  }
+  __syncwarp();
+}
+
+}  // namespace nsk
+}  // namespace muon
