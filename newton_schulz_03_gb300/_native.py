@@ -63,11 +63,12 @@ _lib = None
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:
-    """Load (once) the in-tree shared library; raise if it was not built."""
+    """Load (once) the in-tree shared library (or the one MUON_LIB_PATH
+    names); raise if it was not built."""
     global _lib
     if _lib is not None:
         return _lib
-    p = path or LIB_PATH
+    p = path or os.environ.get("MUON_LIB_PATH") or LIB_PATH
     if not os.path.exists(p):
         raise ImportError(f"{p} is missing: build it with `python -m newton_schulz_03_gb300.build_lib`")
     lib = ctypes.CDLL(p)

@@ -230,6 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
       int mat, ti, tj;
       decode_tile(p, MODE, kBM, BN, t, mat, ti, tj);
+      EpiAux<MODE, BN, true> aux;
+      aux.start(p, mat, ti * kBM + r_tile, ti, tj * BN);   // loads overlap the MMAs
       const bool got = ptx::mbar_wait(&tmem_full[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       epilogue_tile<MODE, BN>(
           p, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN),
-          mat, ti * kBM + r_tile, ti, tj * BN, alpha);
+          mat, ti * kBM + r_tile, aux, alpha);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tmem_empty[acc]);
       acc ^= 1;
@@ -399,10 +401,11 @@ cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out
 cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float b, float c,
                            int* err, int grid_cap, cudaStream_t stream) {
   if (use_pairs(m)) {
-    CUtensorMap t128;
+    CUtensorMap t128, t64;
     cudaError_t e = make_map(&t128, A, m, m, count, kBM);
+    if (e == cudaSuccess) e = make_map(&t64, A, m, m, count, kBK);
     if (e != cudaSuccess) return e;
-    return ns_pair_poly(t128, m, count, A, B_out, b, c, err, grid_cap, stream);
+    return ns_pair_poly(t128, t64, m, count, A, B_out, b, c, err, grid_cap, stream);
   }
   CUtensorMap ta, tab;
   cudaError_t e = make_map(&ta, A, m, m, count, kBM);
@@ -439,7 +442,13 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, 
   // X as the MN-major operand: boxes of 64 columns x 64 K-rows.
   e = make_map(&tx, X, n, m, count, kBK);
   if (e != cudaSuccess) return e;
-  if (use_pairs(m)) return ns_pair_update(tb, tx, m, n, count, X, X_out, a, inv_norm, err, grid_cap, stream);
+  if (use_pairs(m)) {
+    CUtensorMap tb64;
+    e = make_map(&tb64, B, m, m, count, kBK);
+    if (e != cudaSuccess) return e;
+    return ns_pair_update(tb, tb64, tx, m, n, count, X, X_out, a, inv_norm, err, grid_cap,
+                          stream);
+  }
   NsArgs p{};
   p.m = m;
   p.n = n;

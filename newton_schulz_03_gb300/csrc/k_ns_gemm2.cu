@@ -16,9 +16,12 @@
 //   * each CTA's TMEM holds its 128 rows x 256 columns of the accumulator
 //     (two accumulators, 512 columns); both CTAs run the epilogue on their
 //     own rows and report back to the even CTA's "tmem empty" barrier.
-// Symmetric products list only pair tiles (i, j) with i <= j over
-// 256-blocks; inside a diagonal tile the odd CTA skips the 128 x 128
-// sub-block below the diagonal, which the even CTA writes as a mirror.
+// Symmetric products compute AND store only the pair tiles (i, j) with
+// i <= j over 256-blocks (diagonal tiles in full).  Their consumers read a
+// block left of the diagonal, (I, K) with K < I, as the transpose of the
+// stored block (K, I): the producer loads it as an MN-major tile and the
+// MMA takes it through the operand-major bit of the instruction
+// descriptor, chosen per 64-wide K block.  Nothing is stored twice.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -55,7 +58,16 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                        const __grid_constant__ CUtensorMap tmap_b, const NsArgs p) {
+                        const __grid_constant__ CUtensorMap tmap_at,
+                        const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_bt, const NsArgs p) {
+  // A-side operand: rows of X (GRAM), of A (POLY) or of B (UPDATE); A and B
+  // are stored as upper 256-block triangles.  B-side operand: rows of X
+  // (GRAM), of A (POLY), or X as an MN-major operand (UPDATE).
+  // tmap_a / tmap_b: K-major boxes (64 x 128); tmap_at / tmap_bt: 64 x 64
+  // boxes of the same tensors, for blocks read transposed.
+  constexpr bool kSymA = (MODE != kGram);   // A-side source is upper-stored
+  constexpr bool kSymB = (MODE == kPoly);   // B-side source is upper-stored
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -90,6 +102,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmap_a);
     ptx::tma_prefetch_desc(&tmap_b);
+    if (kSymA) ptx::tma_prefetch_desc(&tmap_at);
+    if (kSymB) ptx::tma_prefetch_desc(&tmap_bt);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(tmem_holder, kTmemCols);
@@ -123,11 +137,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (leader) ptx::mbar_arrive_expect_tx(&full[stage], kPairTxBytes);
           uint8_t* sa = smem + stage * kStageBytes;
           uint8_t* sb = sa + kABytes;
-          ptx::tma_load_3d_pair(sa, &tmap_a, full_leader, kb * kBK, rowA, mat);
-          if (MODE == kUpdate) {
+          const int kblk = (kb * kBK) / kPairM;   // 256-block of this K slice
+          if (kSymA && kblk < ti) {
+            // Left of the diagonal: the transpose of stored block (kblk, ti).
 #pragma unroll
             for (int q = 0; q < kHalf / 64; ++q)
-              ptx::tma_load_3d_pair(sb + q * (kBK * 128), &tmap_b, full_leader, colB + q * 64,
+              ptx::tma_load_3d_pair(sa + q * (kBK * 128), &tmap_at, full_leader, rowA + q * 64,
+                                    kb * kBK, mat);
+          } else {
+            ptx::tma_load_3d_pair(sa, &tmap_a, full_leader, kb * kBK, rowA, mat);
+          }
+          if (MODE == kUpdate || (kSymB && kblk < tj)) {
+            // X as the MN-major operand, or the transpose of a stored block.
+            const CUtensorMap* mb = (MODE == kUpdate) ? &tmap_b : &tmap_bt;
+#pragma unroll
+            for (int q = 0; q < kHalf / 64; ++q)
+              ptx::tma_load_3d_pair(sb + q * (kBK * 128), mb, full_leader, colB + q * 64,
                                     kb * kBK, mat);
           } else {
             ptx::tma_load_3d_pair(sb, &tmap_b, full_leader, kb * kBK, colB, mat);
@@ -159,7 +184,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPairM, kPairN, 0, MODE == kUpdate ? 1 : 0);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -171,8 +195,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
+        int mat, ti, tj;
+        decode_tile(p, MODE, kPairM, kPairN, t, mat, ti, tj);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kPairN);
         for (int kb = 0; kb < num_kb; ++kb) {
+          const int kblk = (kb * kBK) / kPairM;
+          const uint32_t a_mn = (kSymA && kblk < ti) ? 1u : 0u;
+          const uint32_t b_mn = (MODE == kUpdate || (kSymB && kblk < tj)) ? 1u : 0u;
+          const uint32_t idesc = ptx::idesc_bf16_f32(kPairM, kPairN, a_mn, b_mn);
           if (!ptx::mbar_wait_cluster(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -182,14 +212,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t adesc = ptx::smem_desc_sw128(sa + k * 32, 16, 1024);
-            uint64_t bdesc;
-            if (MODE == kUpdate) {
-              bdesc = ptx::smem_desc_sw128(sb + k * 16 * 128, kBK * 128, 1024);
-            } else {
-              bdesc = ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
-            }
-            ptx::tc_mma_bf16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            // K-major: a K step of 16 is +32 bytes inside the swizzle row.
+            // MN-major: 64-wide chunks kBK*128 bytes apart, a K step of 16
+            // rows is +2048 bytes.
+            const uint64_t adesc = a_mn ? ptx::smem_desc_sw128(sa + k * 16 * 128, kBK * 128, 1024)
+                                        : ptx::smem_desc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bdesc = b_mn ? ptx::smem_desc_sw128(sb + k * 16 * 128, kBK * 128, 1024)
+                                        : ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
+            ptx::tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           ptx::tc_commit_pair_multicast(&empty[stage], 0x3);  // frees the stage in both CTAs
           if (++stage == kStages) {
@@ -220,6 +250,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int t = pair; t < p.total_tiles; t += npairs) {
       int mat, ti, tj;
       decode_tile(p, MODE, kPairM, kPairN, t, mat, ti, tj);
+      const int rb = ti * (kPairM / kBM) + static_cast<int>(rank);  // 128-row block index
+      EpiAux<MODE, kPairN, false> aux;
+      aux.start(p, mat, rb * kBM + r_tile, rb, tj * kPairN);   // loads overlap the MMAs
       const bool got = ptx::mbar_wait_cluster(&tmem_full[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
@@ -234,10 +267,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float s = p.inv_norm[mat];
         alpha = (MODE == kGram) ? s * s : s;
       }
-      const int rb = ti * (kPairM / kBM) + static_cast<int>(rank);  // 128-row block index
       epilogue_tile<MODE, kPairN>(
           p, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kPairN),
-          mat, rb * kBM + r_tile, rb, tj * kPairN, alpha);
+          mat, rb * kBM + r_tile, aux, alpha);
       ptx::tc_fence_before();
       ptx::mbar_arrive_cluster(acc ? empty_leader1 : empty_leader0);
       acc ^= 1;
@@ -281,14 +313,15 @@ int max_pairs() {
 }
 
 template <int MODE>
-cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const NsArgs& p,
-                        int grid_cap, cudaStream_t stream) {
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tat, const CUtensorMap& tb,
+                        const CUtensorMap& tbt, const NsArgs& p, int grid_cap,
+                        cudaStream_t stream) {
   if (p.total_tiles <= 0) return cudaSuccess;
   int pairs = max_pairs<MODE>();
   if (pairs > grid_cap / 2) pairs = grid_cap / 2;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   if (pairs < 1) pairs = 1;
-  ns_gemm_pair_kernel<MODE><<<2 * pairs, kThreads, kSmemBytes, stream>>>(ta, tb, p);
+  ns_gemm_pair_kernel<MODE><<<2 * pairs, kThreads, kSmemBytes, stream>>>(ta, tat, tb, tbt, p);
   return cudaGetLastError();
 }
 
@@ -318,11 +351,12 @@ cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchVi
   p.out_ms = A_out.ms;
   p.inv_norm = inv_norm;
   p.err = err;
-  return launch_pair<kGram>(tx, tx, p, grid_cap, stream);
+  return launch_pair<kGram>(tx, tx, tx, tx, p, grid_cap, stream);
 }
 
-cudaError_t ns_pair_poly(const CUtensorMap& ta, int m, int count, BatchView A, BatchView B_out,
-                         float b, float c, int* err, int grid_cap, cudaStream_t stream) {
+cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, int count,
+                         BatchView A, BatchView B_out, float b, float c, int* err, int grid_cap,
+                         cudaStream_t stream) {
   NsArgs p{};
   p.m = m;
   p.n = m;
@@ -341,12 +375,12 @@ cudaError_t ns_pair_poly(const CUtensorMap& ta, int m, int count, BatchView A, B
   p.c0 = b;
   p.c1 = c;
   p.err = err;
-  return launch_pair<kPoly>(ta, ta, p, grid_cap, stream);
+  return launch_pair<kPoly>(ta, ta_t, ta, ta_t, p, grid_cap, stream);
 }
 
-cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tx, int m, int n, int count,
-                           BatchView X, BatchView X_out, float a, const float* inv_norm, int* err,
-                           int grid_cap, cudaStream_t stream) {
+cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,
+                           int m, int n, int count, BatchView X, BatchView X_out, float a,
+                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream) {
   NsArgs p{};
   p.m = m;
   p.n = n;
@@ -365,7 +399,7 @@ cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tx, int m, 
   p.inv_norm = inv_norm;
   p.c0 = a;
   p.err = err;
-  return launch_pair<kUpdate>(tb, tx, p, grid_cap, stream);
+  return launch_pair<kUpdate>(tb, tb_t, tx, tx, p, grid_cap, stream);
 }
 
 }  // namespace muon

@@ -69,18 +69,22 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X,
 const char* ns_last_encode_error();
 
 // CTA-pair (cta_group::2) variants of the three products, 256 x 256 tiles;
-// the tensor maps are built by the ns_launch_* functions above.
+// the tensor maps are built by the ns_launch_* functions above (`_t`
+// maps: 64 x 64 boxes of the same tensor, for transposed block reads).
+// A and B produced by the pair kernels hold only their upper 256-block
+// triangle; the pair kernels read them accordingly.
 }  // namespace muon
 #include <cuda.h>
 namespace muon {
 cudaError_t ns_pair_init();
 cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchView A_out,
                          const float* inv_norm, int* err, int grid_cap, cudaStream_t stream);
-cudaError_t ns_pair_poly(const CUtensorMap& ta, int m, int count, BatchView A, BatchView B_out,
-                         float b, float c, int* err, int grid_cap, cudaStream_t stream);
-cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tx, int m, int n, int count,
-                           BatchView X, BatchView X_out, float a, const float* inv_norm, int* err,
-                           int grid_cap, cudaStream_t stream);
+cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, int count,
+                         BatchView A, BatchView B_out, float b, float c, int* err, int grid_cap,
+                         cudaStream_t stream);
+cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,
+                           int m, int n, int count, BatchView X, BatchView X_out, float a,
+                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream);
 
 // Record `msg` as the calling thread's last error text and return `status`
 // (read back through muon_last_error_message).

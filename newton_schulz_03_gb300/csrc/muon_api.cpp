@@ -24,7 +24,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/muon.h"
+#include "muon.h"
 #include "kernels.h"
 
 namespace {

@@ -20,7 +20,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/muon.h"
+#include "muon.h"
 #include "kernels.h"
 
 namespace {

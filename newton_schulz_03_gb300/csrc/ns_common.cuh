@@ -74,35 +74,57 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
 // BN columns col0 .. col0+BN-1, read from TMEM at `taddr` (lane and column
 // already set).  `rb` is the kBM-row block index of the row (symmetric
 // products: a 128-column sub-block left of it is skipped, right of it is
-// also stored mirrored).  The auxiliary operand (A for POLY, X for UPDATE)
-// is prefetched two 32-column chunks ahead.
-template <int MODE, int BN>
-__device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, int mat, int grow,
-                                              int rb, int col0, float alpha) {
-  constexpr int kChunks = BN / 32;
-  const bool row_ok = grow < p.m;
-  __nv_bfloat16* out_m = p.out + static_cast<int64_t>(mat) * p.out_ms;
-  const __nv_bfloat16* aux_row =
-      (MODE == kGram) ? nullptr
-                      : p.aux + static_cast<int64_t>(mat) * p.aux_ms + static_cast<int64_t>(grow) * p.aux_ld;
+// also stored mirrored).
+//
+// With MIRROR the symmetric result is stored in full (sub-blocks left of
+// the diagonal skipped, right of it stored twice); without it only the
+// tile as computed is stored (upper-triangle storage).
+//
+// The auxiliary operand (A for POLY, X for UPDATE) does not depend on the
+// accumulator, so its first kPrefetch chunks are loaded before the wait
+// for the accumulator (EpiAux::start) and the rest kPrefetch chunks ahead.
+template <int MODE, int BN, bool MIRROR>
+struct EpiAux {
+  static constexpr int kChunks = BN / 32;
+  static constexpr int kPrefetch = (kChunks < 4) ? kChunks : 4;
+  uint4 pre[kPrefetch][4];
+  const __nv_bfloat16* row;   // aux row of this thread (NULL for GRAM)
+  int col0, rb;
+  bool row_ok;
+  int out_cols;
 
-  auto chunk_live = [&](int cb) {
+  __device__ __forceinline__ bool live(int cb) const {
     const int g0 = col0 + cb * 32;
-    const bool below = (MODE != kUpdate) && (g0 / kBM < rb);
-    return row_ok && g0 < p.out_cols && !below;
-  };
-  auto chunk_full = [&](int cb) { return col0 + cb * 32 + 32 <= p.out_cols; };
-
-  uint4 pre[2][4];
-  auto prefetch = [&](int cb, uint4 (&dst)[4]) {
-    if (MODE != kGram && cb < kChunks && chunk_live(cb) && chunk_full(cb)) {
-      const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0 + cb * 32);
+    const bool below = MIRROR && (MODE != kUpdate) && (g0 / kBM < rb);
+    return row_ok && g0 < out_cols && !below;
+  }
+  __device__ __forceinline__ bool full(int cb) const { return col0 + cb * 32 + 32 <= out_cols; }
+  __device__ __forceinline__ void load(int cb) {
+    if (MODE != kGram && cb < kChunks && live(cb) && full(cb)) {
+      const uint4* src = reinterpret_cast<const uint4*>(row + col0 + cb * 32);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = __ldg(src + q);
+      for (int q = 0; q < 4; ++q) pre[cb % kPrefetch][q] = __ldg(src + q);
     }
-  };
-  prefetch(0, pre[0]);
-  prefetch(1, pre[1]);
+  }
+  __device__ __forceinline__ void start(const NsArgs& p, int mat, int grow, int rb_, int col0_) {
+    col0 = col0_;
+    rb = rb_;
+    row_ok = grow < p.m;
+    out_cols = p.out_cols;
+    row = (MODE == kGram) ? nullptr
+                          : p.aux + static_cast<int64_t>(mat) * p.aux_ms +
+                                static_cast<int64_t>(grow) * p.aux_ld;
+#pragma unroll
+    for (int cb = 0; cb < kPrefetch; ++cb) load(cb);
+  }
+};
+
+template <int MODE, int BN, bool MIRROR>
+__device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, int mat, int grow,
+                                              EpiAux<MODE, BN, MIRROR>& aux, float alpha) {
+  constexpr int kChunks = BN / 32;
+  constexpr int kPre = EpiAux<MODE, BN, MIRROR>::kPrefetch;
+  __nv_bfloat16* out_m = p.out + static_cast<int64_t>(mat) * p.out_ms;
 
 #pragma unroll
   for (int cb = 0; cb < kChunks; ++cb) {
@@ -110,10 +132,10 @@ __device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, i
     __syncwarp();  // tcgen05.ld is warp-collective: keep the warp converged
     ptx::tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cb * 32), v);
     ptx::tmem_ld_wait();
-    const int gcol0 = col0 + cb * 32;
-    if (chunk_live(cb)) {
-      const bool full_chunk = chunk_full(cb);
-      const bool mirror = (MODE != kUpdate) && (gcol0 / kBM > rb);
+    const int gcol0 = aux.col0 + cb * 32;
+    if (aux.live(cb)) {
+      const bool full_chunk = aux.full(cb);
+      const bool mirror = MIRROR && (MODE != kUpdate) && (gcol0 / kBM > aux.rb);
       float f[32];
       if (MODE == kGram) {
 #pragma unroll
@@ -123,14 +145,14 @@ __device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, i
         if (full_chunk) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 u = pre[cb & 1][q];
+            const uint4 u = aux.pre[cb % kPre][q];
             x[q * 8 + 0] = bf16lo(u.x); x[q * 8 + 1] = bf16hi(u.x);
             x[q * 8 + 2] = bf16lo(u.y); x[q * 8 + 3] = bf16hi(u.y);
             x[q * 8 + 4] = bf16lo(u.z); x[q * 8 + 5] = bf16hi(u.z);
             x[q * 8 + 6] = bf16lo(u.w); x[q * 8 + 7] = bf16hi(u.w);
           }
         } else {
-          const uint16_t* a16 = reinterpret_cast<const uint16_t*>(aux_row + gcol0);
+          const uint16_t* a16 = reinterpret_cast<const uint16_t*>(aux.row + gcol0);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             x[e] = (gcol0 + e < p.out_cols) ? __uint_as_float(static_cast<uint32_t>(a16[e]) << 16)
@@ -170,7 +192,7 @@ __device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, i
             o16[static_cast<int64_t>(gcol0 + e) * p.out_ld + grow] = to_bf16_bits(f[e]);
       }
     }
-    prefetch(cb + 2, pre[cb & 1]);
+    aux.load(cb + kPre);
   }
   __syncwarp();
 }
