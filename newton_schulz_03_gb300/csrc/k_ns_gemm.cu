@@ -317,6 +317,31 @@ cudaError_t make_map(CUtensorMap* map, BatchView v, int cols, int rows, int coun
   return cudaSuccess;
 }
 
+// 4-D view of a batch for MN-major operand tiles: (64 columns, rows,
+// 64-column chunks, matrix).  A box (64, 64, chunks, 1) lands in shared
+// memory as `chunks` consecutive 64 x 64 swizzled blocks -- the layout the
+// MN-major descriptor expects -- in one copy.  Needs cols % 64 == 0.
+cudaError_t make_map_mn4d(CUtensorMap* map, BatchView v, int cols, int rows, int count,
+                          int chunks) {
+  EncodeFn enc = get_encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64),
+                              static_cast<cuuint64_t>(count)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(v.ld) * 2, 128u,
+                                 static_cast<cuuint64_t>(v.ms) * 2};
+  const cuuint32_t box[4] = {64u, 64u, static_cast<cuuint32_t>(chunks), 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v.ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_encode_err, sizeof(g_encode_err), "4-D map encode failed (%d)", static_cast<int>(r));
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 template <int MODE, int BN>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const NsArgs& p, int grid_cap,
                    cudaStream_t stream) {
@@ -402,10 +427,12 @@ cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float
                            int* err, int grid_cap, cudaStream_t stream) {
   if (use_pairs(m)) {
     CUtensorMap t128, t64;
+    const int mn4d = (m % 64 == 0) ? 1 : 0;
     cudaError_t e = make_map(&t128, A, m, m, count, kBM);
-    if (e == cudaSuccess) e = make_map(&t64, A, m, m, count, kBK);
+    if (e == cudaSuccess)
+      e = mn4d ? make_map_mn4d(&t64, A, m, m, count, 2) : make_map(&t64, A, m, m, count, kBK);
     if (e != cudaSuccess) return e;
-    return ns_pair_poly(t128, t64, m, count, A, B_out, b, c, err, grid_cap, stream);
+    return ns_pair_poly(t128, t64, m, count, A, B_out, b, c, err, grid_cap, stream, mn4d);
   }
   CUtensorMap ta, tab;
   cudaError_t e = make_map(&ta, A, m, m, count, kBM);
@@ -443,11 +470,18 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, 
   e = make_map(&tx, X, n, m, count, kBK);
   if (e != cudaSuccess) return e;
   if (use_pairs(m)) {
-    CUtensorMap tb64;
-    e = make_map(&tb64, B, m, m, count, kBK);
+    CUtensorMap tb64, tx4;
+    const int mn4d = (m % 64 == 0 && n % 64 == 0) ? 1 : 0;
+    if (mn4d) {
+      e = make_map_mn4d(&tb64, B, m, m, count, 2);
+      if (e == cudaSuccess) e = make_map_mn4d(&tx4, X, n, m, count, 2);
+    } else {
+      e = make_map(&tb64, B, m, m, count, kBK);
+      tx4 = tx;
+    }
     if (e != cudaSuccess) return e;
-    return ns_pair_update(tb, tb64, tx, m, n, count, X, X_out, a, inv_norm, err, grid_cap,
-                          stream);
+    return ns_pair_update(tb, tb64, tx4, m, n, count, X, X_out, a, inv_norm, err, grid_cap,
+                          stream, mn4d);
   }
   NsArgs p{};
   p.m = m;

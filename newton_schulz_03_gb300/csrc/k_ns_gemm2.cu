@@ -22,6 +22,10 @@
 // stored block (K, I): the producer loads it as an MN-major tile and the
 // MMA takes it through the operand-major bit of the instruction
 // descriptor, chosen per 64-wide K block.  Nothing is stored twice.
+// MN-major tiles (these transposed blocks and the X operand of the update)
+// are fetched with one copy through a 4-D view of the matrix (64 columns,
+// rows, 64-column chunks, matrix) when the column count is a multiple of
+// 64; otherwise as one 64 x 64 box per chunk.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -140,20 +144,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int kblk = (kb * kBK) / kPairM;   // 256-block of this K slice
           if (kSymA && kblk < ti) {
             // Left of the diagonal: the transpose of stored block (kblk, ti).
+            if (p.mn4d) {
+              ptx::tma_load_4d_pair(sa, &tmap_at, full_leader, 0, kb * kBK, rowA / 64, mat);
+            } else {
 #pragma unroll
-            for (int q = 0; q < kHalf / 64; ++q)
-              ptx::tma_load_3d_pair(sa + q * (kBK * 128), &tmap_at, full_leader, rowA + q * 64,
-                                    kb * kBK, mat);
+              for (int q = 0; q < kHalf / 64; ++q)
+                ptx::tma_load_3d_pair(sa + q * (kBK * 128), &tmap_at, full_leader, rowA + q * 64,
+                                      kb * kBK, mat);
+            }
           } else {
             ptx::tma_load_3d_pair(sa, &tmap_a, full_leader, kb * kBK, rowA, mat);
           }
           if (MODE == kUpdate || (kSymB && kblk < tj)) {
             // X as the MN-major operand, or the transpose of a stored block.
             const CUtensorMap* mb = (MODE == kUpdate) ? &tmap_b : &tmap_bt;
+            if (p.mn4d) {
+              ptx::tma_load_4d_pair(sb, mb, full_leader, 0, kb * kBK, colB / 64, mat);
+            } else {
 #pragma unroll
-            for (int q = 0; q < kHalf / 64; ++q)
-              ptx::tma_load_3d_pair(sb + q * (kBK * 128), mb, full_leader, colB + q * 64,
-                                    kb * kBK, mat);
+              for (int q = 0; q < kHalf / 64; ++q)
+                ptx::tma_load_3d_pair(sb + q * (kBK * 128), mb, full_leader, colB + q * 64,
+                                      kb * kBK, mat);
+            }
           } else {
             ptx::tma_load_3d_pair(sb, &tmap_b, full_leader, kb * kBK, colB, mat);
           }
@@ -356,8 +368,9 @@ cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchVi
 
 cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, int count,
                          BatchView A, BatchView B_out, float b, float c, int* err, int grid_cap,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int mn4d) {
   NsArgs p{};
+  p.mn4d = mn4d;
   p.m = m;
   p.n = m;
   p.K = m;
@@ -380,8 +393,10 @@ cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, 
 
 cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,
                            int m, int n, int count, BatchView X, BatchView X_out, float a,
-                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream) {
+                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream,
+                           int mn4d) {
   NsArgs p{};
+  p.mn4d = mn4d;
   p.m = m;
   p.n = n;
   p.K = m;

@@ -34,6 +34,7 @@ struct NsArgs {
   const float* inv_norm;      // alpha source (NULL: alpha = 1)
   float c0, c1;               // POLY: (b, c); UPDATE: (a, unused)
   int* err;
+  int32_t mn4d;               // MN-major operand maps are 4-D chunk views (one copy per operand)
 };
 
 // Tile t -> (matrix, row tile, column tile).  Symmetric products list, per

@@ -220,6 +220,17 @@ __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const void* tma
       : "memory");
 }
 
+// 4-D variant (coordinates x, y, z, w).
+__device__ __forceinline__ void tma_load_4d_pair(void* smem_dst, const void* tmap,
+                                                 uint32_t bar_cluster_addr, int32_t x, int32_t y,
+                                                 int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster_addr), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // tcgen05 for a CTA pair (cta_group::2).  alloc/dealloc/relinquish are
 // executed by one warp in each of the two CTAs; the MMA and its commits by
 // one thread of the even CTA.
