@@ -209,10 +209,14 @@ struct muon_handle_s {
   void* ws = nullptr;
   size_t ws_size = 0;
   int* dev_err = nullptr;
+  // Host-buffer step: device staging ring, copy streams and their events.
   float* staging = nullptr;
   size_t staging_bytes = 0;
-  // ns entry point scratch: one extra X buffer plus A and B
-  // (lives in the workspace).
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t entry_ev = nullptr;
+  cudaEvent_t slot_in[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t slot_comp[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t slot_out[3] = {nullptr, nullptr, nullptr};
   bool timing = false;
   struct Pending {
     int kind;
@@ -439,6 +443,14 @@ muon_status_t muon_destroy(muon_handle_t h) {
   for (cudaEvent_t e : h->free_events) cudaEventDestroy(e);
   if (h->ws) cudaFree(h->ws);
   if (h->staging) cudaFree(h->staging);
+  if (h->copy_in) cudaStreamDestroy(h->copy_in);
+  if (h->copy_out) cudaStreamDestroy(h->copy_out);
+  if (h->entry_ev) cudaEventDestroy(h->entry_ev);
+  for (int i = 0; i < 3; ++i) {
+    if (h->slot_in[i]) cudaEventDestroy(h->slot_in[i]);
+    if (h->slot_comp[i]) cudaEventDestroy(h->slot_comp[i]);
+    if (h->slot_out[i]) cudaEventDestroy(h->slot_out[i]);
+  }
   if (h->dev_err) cudaFree(h->dev_err);
   delete h;
   return MUON_OK;
@@ -540,23 +552,47 @@ muon_status_t muon_step_host(muon_handle_t h, const muon_group_t* groups, int32_
                              float* const* momentum_host, const float* const* grad_host,
                              float* const* weights_host, float lr, float wd, float mu,
                              int32_t ns_steps, void* stream) {
+  // Pipeline over pieces of at most kPieceBytes of state: while piece k is
+  // stepped on `stream`, piece k+1 is copied in on one copy stream and
+  // piece k-1 is copied out on another.  A ring of three device slots holds
+  // the pieces' momentum, gradient and weights.
+  constexpr size_t kPieceBytes = size_t(384) << 20;
+  constexpr int kSlots = 3;
   muon_status_t st = check_handle(h);
   if (st != MUON_OK) return st;
   st = validate_groups(groups, n_groups);
   if (st != MUON_OK) return st;
+  if (!finite3(lr, wd, mu)) return fail(MUON_ERR_INVALID_ARG, "lr, wd and mu must be finite");
+  if (ns_steps < 0 || ns_steps > kMaxSteps)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps out of range (%d)", ns_steps);
   if (n_groups > 0 && (momentum_host == nullptr || grad_host == nullptr || weights_host == nullptr))
     return fail(MUON_ERR_INVALID_ARG, "pointer arrays must not be NULL");
-  size_t total = 0;
-  std::vector<size_t> offs(n_groups);
   for (int g = 0; g < n_groups; ++g) {
-    offs[g] = total;
-    const size_t ne = size_t(groups[g].rows) * groups[g].cols * groups[g].count;
-    if (ne > 0 && (momentum_host[g] == nullptr || grad_host[g] == nullptr ||
-                   weights_host[g] == nullptr))
+    if (groups[g].count == 0) continue;
+    if (momentum_host[g] == nullptr || grad_host[g] == nullptr || weights_host[g] == nullptr)
       return fail(MUON_ERR_INVALID_ARG, "group %d: NULL host buffer", g);
-    total += align_up(ne, 64);  // 256-byte aligned group slices
   }
-  const size_t bytes = 3 * total * sizeof(float);
+
+  // Pieces: consecutive runs of matrices of one group.
+  struct Piece {
+    int group;
+    int64_t first;
+    int count;
+  };
+  std::vector<Piece> pieces;
+  size_t slot_elems = 64;
+  for (int g = 0; g < n_groups; ++g) {
+    const int64_t per = int64_t(groups[g].rows) * groups[g].cols;
+    int64_t take = std::max<int64_t>(1, static_cast<int64_t>(kPieceBytes / (12 * size_t(per))));
+    for (int64_t first = 0; first < groups[g].count; first += take) {
+      const int c = static_cast<int>(std::min<int64_t>(take, groups[g].count - first));
+      pieces.push_back({g, first, c});
+      slot_elems = std::max(slot_elems, align_up(size_t(per) * c, 64));
+    }
+  }
+  if (pieces.empty()) return MUON_OK;
+
+  const size_t bytes = size_t(kSlots) * 3 * slot_elems * sizeof(float);
   if (h->staging_bytes < bytes) {
     if (h->staging) {
       cudaDeviceSynchronize();
@@ -571,33 +607,60 @@ muon_status_t muon_step_host(muon_handle_t h, const muon_group_t* groups, int32_
     }
     h->staging_bytes = bytes;
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  std::vector<float*> dm(n_groups), dw(n_groups);
-  std::vector<const float*> dg(n_groups);
-  for (int g = 0; g < n_groups; ++g) {
-    const size_t ne = size_t(groups[g].rows) * groups[g].cols * groups[g].count;
-    dm[g] = h->staging + offs[g];
-    dg[g] = h->staging + total + offs[g];
-    dw[g] = h->staging + 2 * total + offs[g];
-    if (ne == 0) continue;
-    cudaError_t e = cudaMemcpyAsync(dm[g], momentum_host[g], ne * 4, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(const_cast<float*>(dg[g]), grad_host[g], ne * 4, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(dw[g], weights_host[g], ne * 4, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+  if (h->copy_in == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->entry_ev, cudaEventDisableTiming);
+    for (int i = 0; i < kSlots && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&h->slot_in[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slot_comp[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slot_out[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "copy stream set-up");
   }
-  st = muon_step(h, groups, n_groups, dm.data(), dg.data(), dw.data(), lr, wd, mu, ns_steps, stream);
-  if (st != MUON_OK) return st;
-  for (int g = 0; g < n_groups; ++g) {
-    const size_t ne = size_t(groups[g].rows) * groups[g].cols * groups[g].count;
-    if (ne == 0) continue;
-    cudaError_t e = cudaMemcpyAsync(momentum_host[g], dm[g], ne * 4, cudaMemcpyDeviceToHost, s);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaEventRecord(h->entry_ev, s);  // order after prior work on `stream`
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->copy_in, h->entry_ev, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->copy_out, h->entry_ev, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "stream ordering");
+
+  for (size_t k = 0; k < pieces.size(); ++k) {
+    const Piece& pc = pieces[k];
+    const int slot = static_cast<int>(k % kSlots);
+    const muon_group_t& G = groups[pc.group];
+    const size_t ne = size_t(G.rows) * G.cols * pc.count;
+    const size_t off = size_t(pc.first) * G.rows * G.cols;
+    float* dM = h->staging + size_t(slot) * 3 * slot_elems;
+    float* dG = dM + slot_elems;
+    float* dW = dG + slot_elems;
+    // Copy in once the slot's previous piece has been copied out.
+    if (k >= static_cast<size_t>(kSlots)) e = cudaStreamWaitEvent(h->copy_in, h->slot_out[slot], 0);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(weights_host[g], dw[g], ne * 4, cudaMemcpyDeviceToHost, s);
+      e = cudaMemcpyAsync(dM, momentum_host[pc.group] + off, ne * 4, cudaMemcpyHostToDevice, h->copy_in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dG, grad_host[pc.group] + off, ne * 4, cudaMemcpyHostToDevice, h->copy_in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dW, weights_host[pc.group] + off, ne * 4, cudaMemcpyHostToDevice, h->copy_in);
+    if (e == cudaSuccess) e = cudaEventRecord(h->slot_in[slot], h->copy_in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->slot_in[slot], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    const muon_group_t pg{G.rows, G.cols, pc.count, G.update_scale};
+    float* pm[1] = {dM};
+    const float* pgr[1] = {dG};
+    float* pw[1] = {dW};
+    st = muon_step(h, &pg, 1, pm, pgr, pw, lr, wd, mu, ns_steps, stream);
+    if (st != MUON_OK) return st;
+    e = cudaEventRecord(h->slot_comp[slot], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->copy_out, h->slot_comp[slot], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(momentum_host[pc.group] + off, dM, ne * 4, cudaMemcpyDeviceToHost, h->copy_out);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(weights_host[pc.group] + off, dW, ne * 4, cudaMemcpyDeviceToHost, h->copy_out);
+    if (e == cudaSuccess) e = cudaEventRecord(h->slot_out[slot], h->copy_out);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
   }
-  cudaError_t e = cudaStreamSynchronize(s);
+  e = cudaStreamSynchronize(h->copy_out);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   return MUON_OK;
 }

@@ -293,3 +293,24 @@ def test_kernel_timing_counts_launches(ns, h):
     assert st["total_launches"] == 18
     assert all(v >= 0.0 for v in st["total_ms"].values())
     assert st["total_ms"]["ns_update"] > 0.0
+
+
+def test_step_host_pipeline_matches_device_step(ns, h):
+    """Host-buffer step over several pipeline pieces (>384 MB of state)
+    equals the device-buffer step bit for bit, and sampled matrices match
+    the oracle."""
+    rng = np.random.default_rng(12)
+    r, c, k = 1024, 1024, 40
+    W, M, G = (rng.standard_normal((k, r, c), dtype=np.float32) * np.float32(0.05)
+               for _ in range(3))
+    Wh, Mh, Gh = (torch.from_numpy(a.copy()).pin_memory() for a in (W, M, G))
+    ns.muon_step_host(h, [(r, c, k)], [Mh], [Gh], [Wh], 0.02, 0.1, 0.95, 5)
+    dW, dM, dG = dev(W), dev(M), dev(G)
+    ns.muon_step(h, [(r, c, k)], [dM], [dG], [dW], 0.02, 0.1, 0.95, 5)
+    ns.muon_last_device_error(h)
+    np.testing.assert_array_equal(Mh.numpy(), dM.cpu().numpy())
+    np.testing.assert_array_equal(Wh.numpy(), dW.cpu().numpy())
+    for i in (0, 39):
+        st = o.muon_step_matrix(W[i], M[i], G[i], lr=0.02, wd=0.1, mu=0.95)
+        err = np.linalg.norm(Wh.numpy()[i].astype(np.float64) - st.W_new) / (0.02 * np.linalg.norm(st.O))
+        assert err <= NS_TOL + 1e-3
