@@ -9,9 +9,10 @@
 // products, each one launch of the kernel below over a whole batch of
 // same-shape matrices:
 //
-//   GRAM    A  = alpha X X^T        K = n   symmetric: upper tiles + mirror
-//   POLY    B  = b A + c A A        K = m   symmetric: upper tiles + mirror
-//   UPDATE  X' = alpha (a X + B X)  K = m   all tiles
+//   GRAM    A  = alpha X X^T          K = n   symmetric
+//   POLY    B' = a I + b A + c A A    K = m   symmetric
+//   UPDATE  X' = alpha B' X           K = m   all tiles
+// (the linear term a X of the quintic is folded into the diagonal of B').
 //
 // alpha folds the Frobenius pre-normalisation into the first iteration
 // (alpha = 1/s^2 for the Gram product and 1/s for the update).
@@ -423,8 +424,8 @@ cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out
   return launch<kGram, kSymBN>(tx, txb, p, grid_cap, stream);
 }
 
-cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float b, float c,
-                           int* err, int grid_cap, cudaStream_t stream) {
+cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float a, float b,
+                           float c, int* err, int grid_cap, cudaStream_t stream) {
   if (use_pairs(m)) {
     CUtensorMap t128, t64;
     const int mn4d = (m % 64 == 0) ? 1 : 0;
@@ -432,7 +433,7 @@ cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float
     if (e == cudaSuccess)
       e = mn4d ? make_map_mn4d(&t64, A, m, m, count, 2) : make_map(&t64, A, m, m, count, kBK);
     if (e != cudaSuccess) return e;
-    return ns_pair_poly(t128, t64, m, count, A, B_out, b, c, err, grid_cap, stream, mn4d);
+    return ns_pair_poly(t128, t64, m, count, A, B_out, a, b, c, err, grid_cap, stream, mn4d);
   }
   CUtensorMap ta, tab;
   cudaError_t e = make_map(&ta, A, m, m, count, kBM);
@@ -456,13 +457,13 @@ cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float
   p.inv_norm = nullptr;
   p.c0 = b;
   p.c1 = c;
+  p.c2 = a;
   p.err = err;
   return launch<kPoly, kSymBN>(ta, tab, p, grid_cap, stream);
 }
 
 cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, BatchView X_out,
-                             float a, const float* inv_norm, int* err, int grid_cap,
-                             cudaStream_t stream) {
+                             const float* inv_norm, int* err, int grid_cap, cudaStream_t stream) {
   CUtensorMap tb, tx;
   cudaError_t e = make_map(&tb, B, m, m, count, kBM);
   if (e != cudaSuccess) return e;
@@ -480,8 +481,8 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, 
       tx4 = tx;
     }
     if (e != cudaSuccess) return e;
-    return ns_pair_update(tb, tb64, tx4, m, n, count, X, X_out, a, inv_norm, err, grid_cap,
-                          stream, mn4d);
+    return ns_pair_update(tb, tb64, tx4, m, n, count, X_out, inv_norm, err, grid_cap, stream,
+                          mn4d);
   }
   NsArgs p{};
   p.m = m;
@@ -495,11 +496,7 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, 
   p.out = static_cast<__nv_bfloat16*>(const_cast<void*>(X_out.ptr));
   p.out_ld = X_out.ld;
   p.out_ms = X_out.ms;
-  p.aux = static_cast<const __nv_bfloat16*>(X.ptr);
-  p.aux_ld = X.ld;
-  p.aux_ms = X.ms;
   p.inv_norm = inv_norm;
-  p.c0 = a;
   p.err = err;
   return launch<kUpdate, kUpdBN>(tb, tx, p, grid_cap, stream);
 }

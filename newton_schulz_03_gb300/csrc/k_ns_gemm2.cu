@@ -2,7 +2,7 @@
 // cta_group::2), 256 x 256 output tiles per pair.
 //
 // Same three products as k_ns_gemm.cu (Gram A = alpha X X^T, square
-// B = b A + c A A, update X' = alpha (a X + B X); "Frontier Pre-training at
+// B' = a I + b A + c A A, update X' = alpha B' X; "Frontier Pre-training at
 // Microsoft AI", Method details §5, resharding step 3), scheduled on
 // clusters of two CTAs on two SMs:
 //   * each CTA stages its own 128-row half of the A-side operand and its own
@@ -367,8 +367,8 @@ cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchVi
 }
 
 cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, int count,
-                         BatchView A, BatchView B_out, float b, float c, int* err, int grid_cap,
-                         cudaStream_t stream, int mn4d) {
+                         BatchView A, BatchView B_out, float a, float b, float c, int* err,
+                         int grid_cap, cudaStream_t stream, int mn4d) {
   NsArgs p{};
   p.mn4d = mn4d;
   p.m = m;
@@ -387,14 +387,14 @@ cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, 
   p.aux_ms = A.ms;
   p.c0 = b;
   p.c1 = c;
+  p.c2 = a;
   p.err = err;
   return launch_pair<kPoly>(ta, ta_t, ta, ta_t, p, grid_cap, stream);
 }
 
 cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,
-                           int m, int n, int count, BatchView X, BatchView X_out, float a,
-                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream,
-                           int mn4d) {
+                           int m, int n, int count, BatchView X_out, const float* inv_norm,
+                           int* err, int grid_cap, cudaStream_t stream, int mn4d) {
   NsArgs p{};
   p.mn4d = mn4d;
   p.m = m;
@@ -408,11 +408,7 @@ cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const
   p.out = static_cast<__nv_bfloat16*>(const_cast<void*>(X_out.ptr));
   p.out_ld = X_out.ld;
   p.out_ms = X_out.ms;
-  p.aux = static_cast<const __nv_bfloat16*>(X.ptr);
-  p.aux_ld = X.ld;
-  p.aux_ms = X.ms;
   p.inv_norm = inv_norm;
-  p.c0 = a;
   p.err = err;
   return launch_pair<kUpdate>(tb, tb_t, tx, tx, p, grid_cap, stream);
 }

@@ -56,14 +56,15 @@ cudaError_t ns_gemm_init();
 cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out,
                            const float* inv_norm, int* err, int grid_cap, cudaStream_t stream);
 
-// B = b A + c A A (A symmetric m x m).  Upper-triangle tiles only, mirrored.
-cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float b, float c,
-                           int* err, int grid_cap, cudaStream_t stream);
+// B' = a I + b A + c A A (A symmetric m x m): the quintic polynomial with
+// the linear term folded in.  Upper-triangle tiles only.
+cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float a, float b,
+                           float c, int* err, int grid_cap, cudaStream_t stream);
 
-// X' = alpha (a X + B X), alpha = inv_norm[mat] (or 1 when NULL).
+// X' = alpha B' X, alpha = inv_norm[mat] (or 1 when NULL).
 cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X,
-                             BatchView X_out, float a, const float* inv_norm, int* err,
-                             int grid_cap, cudaStream_t stream);
+                             BatchView X_out, const float* inv_norm, int* err, int grid_cap,
+                             cudaStream_t stream);
 
 // Last error text of a tensor-map encode (host, thread-local).
 const char* ns_last_encode_error();
@@ -80,12 +81,11 @@ cudaError_t ns_pair_init();
 cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchView A_out,
                          const float* inv_norm, int* err, int grid_cap, cudaStream_t stream);
 cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, int count,
-                         BatchView A, BatchView B_out, float b, float c, int* err, int grid_cap,
-                         cudaStream_t stream, int mn4d);
+                         BatchView A, BatchView B_out, float a, float b, float c, int* err,
+                         int grid_cap, cudaStream_t stream, int mn4d);
 cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,
-                           int m, int n, int count, BatchView X, BatchView X_out, float a,
-                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream,
-                           int mn4d);
+                           int m, int n, int count, BatchView X_out, const float* inv_norm,
+                           int* err, int grid_cap, cudaStream_t stream, int mn4d);
 
 // Record `msg` as the calling thread's last error text and return `status`
 // (read back through muon_last_error_message).

@@ -318,13 +318,13 @@ muon_status_t run_newton_schulz(muon_handle_t h, int m, int n, int count, muon::
                                       muon::ns_last_encode_error());
     {
       LaunchScope L(h, MUON_KERNEL_NS_POLY, s);
-      e = muon::ns_launch_poly(m, count, A, B, co.b, co.c, h->dev_err, h->num_sms, s);
+      e = muon::ns_launch_poly(m, count, A, B, co.a, co.b, co.c, h->dev_err, h->num_sms, s);
     }
     if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "poly launch: %s %s", cudaGetErrorString(e),
                                       muon::ns_last_encode_error());
     {
       LaunchScope L(h, MUON_KERNEL_NS_UPDATE, s);
-      e = muon::ns_launch_update(m, n, count, B, src, dst, co.a, inv, h->dev_err, h->num_sms, s);
+      e = muon::ns_launch_update(m, n, count, B, src, dst, inv, h->dev_err, h->num_sms, s);
     }
     if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "update launch: %s %s",
                                       cudaGetErrorString(e), muon::ns_last_encode_error());

@@ -142,8 +142,8 @@ extern "C" muon_status_t muon_newton_schulz_bf16_static(int32_t m, int32_t n, in
       const muon::BatchView dst = (((ns_steps - 1 - k) % 2) == 0) ? vo : vt;
       const float* alpha = (k == 0) ? inv : nullptr;
       e = muon::ns_launch_gram(m, n, take, src, vA, alpha, err, sms, s);
-      if (e == cudaSuccess) e = muon::ns_launch_poly(m, take, vA, vB, b, c, err, sms, s);
-      if (e == cudaSuccess) e = muon::ns_launch_update(m, n, take, vB, src, dst, a, alpha, err, sms, s);
+      if (e == cudaSuccess) e = muon::ns_launch_poly(m, take, vA, vB, a, b, c, err, sms, s);
+      if (e == cudaSuccess) e = muon::ns_launch_update(m, n, take, vB, src, dst, alpha, err, sms, s);
       src = dst;
     }
     if (e != cudaSuccess) return fail_s(MUON_ERR_CUDA, "Newton-Schulz launch failed");

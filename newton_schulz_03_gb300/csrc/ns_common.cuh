@@ -29,10 +29,10 @@ struct NsArgs {
   int32_t out_cols;           // columns of the output matrix
   __nv_bfloat16* out;
   int64_t out_ld, out_ms;
-  const __nv_bfloat16* aux;   // POLY: A; UPDATE: X
+  const __nv_bfloat16* aux;   // POLY: A (the only product with an auxiliary operand)
   int64_t aux_ld, aux_ms;
   const float* inv_norm;      // alpha source (NULL: alpha = 1)
-  float c0, c1;               // POLY: (b, c); UPDATE: (a, unused)
+  float c0, c1, c2;           // POLY: (b, c, a): B' = a I + b A + c A A
   int* err;
   int32_t mn4d;               // MN-major operand maps are 4-D chunk views (one copy per operand)
 };
@@ -81,7 +81,7 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
 // the diagonal skipped, right of it stored twice); without it only the
 // tile as computed is stored (upper-triangle storage).
 //
-// The auxiliary operand (A for POLY, X for UPDATE) does not depend on the
+// The auxiliary operand (A, read by POLY only) does not depend on the
 // accumulator, so its first kPrefetch chunks are loaded before the wait
 // for the accumulator (EpiAux::start) and the rest kPrefetch chunks ahead.
 template <int MODE, int BN, bool MIRROR>
@@ -89,7 +89,7 @@ struct EpiAux {
   static constexpr int kChunks = BN / 32;
   static constexpr int kPrefetch = (kChunks < 4) ? kChunks : 4;
   uint4 pre[kPrefetch][4];
-  const __nv_bfloat16* row;   // aux row of this thread (NULL for GRAM)
+  const __nv_bfloat16* row;   // aux row of this thread (POLY only)
   int col0, rb;
   bool row_ok;
   int out_cols;
@@ -101,7 +101,7 @@ struct EpiAux {
   }
   __device__ __forceinline__ bool full(int cb) const { return col0 + cb * 32 + 32 <= out_cols; }
   __device__ __forceinline__ void load(int cb) {
-    if (MODE != kGram && cb < kChunks && live(cb) && full(cb)) {
+    if (MODE == kPoly && cb < kChunks && live(cb) && full(cb)) {
       const uint4* src = reinterpret_cast<const uint4*>(row + col0 + cb * 32);
 #pragma unroll
       for (int q = 0; q < 4; ++q) pre[cb % kPrefetch][q] = __ldg(src + q);
@@ -112,7 +112,7 @@ struct EpiAux {
     rb = rb_;
     row_ok = grow < p.m;
     out_cols = p.out_cols;
-    row = (MODE == kGram) ? nullptr
+    row = (MODE != kPoly) ? nullptr
                           : p.aux + static_cast<int64_t>(mat) * p.aux_ms +
                                 static_cast<int64_t>(grow) * p.aux_ld;
 #pragma unroll
@@ -138,7 +138,9 @@ __device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, i
       const bool full_chunk = aux.full(cb);
       const bool mirror = MIRROR && (MODE != kUpdate) && (gcol0 / kBM > aux.rb);
       float f[32];
-      if (MODE == kGram) {
+      if (MODE != kPoly) {
+        // Gram: alpha X X^T.  Update: alpha (a I + b A + c A^2) X, the a X
+        // term being folded into the square product's diagonal.
 #pragma unroll
         for (int e = 0; e < 32; ++e) f[e] = alpha * __uint_as_float(v[e]);
       } else {
@@ -159,12 +161,11 @@ __device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, i
             x[e] = (gcol0 + e < p.out_cols) ? __uint_as_float(static_cast<uint32_t>(a16[e]) << 16)
                                             : 0.f;
         }
-        if (MODE == kPoly) {
+        // B' = b A + c A^2, plus a on the diagonal.
 #pragma unroll
-          for (int e = 0; e < 32; ++e) f[e] = fmaf(p.c1, __uint_as_float(v[e]), p.c0 * x[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) f[e] = alpha * fmaf(p.c0, x[e], __uint_as_float(v[e]));
+        for (int e = 0; e < 32; ++e) {
+          const float d = (gcol0 + e == grow) ? p.c2 : 0.f;
+          f[e] = fmaf(p.c1, __uint_as_float(v[e]), fmaf(p.c0, x[e], d));
         }
       }
       __nv_bfloat16* orow = out_m + static_cast<int64_t>(grow) * p.out_ld + gcol0;

@@ -154,8 +154,10 @@ def newton_schulz(X: np.ndarray, s: float, steps: int = NS_STEPS,
     X0 = X / s; then ``steps`` times:  A = X X^T,  B = b A + c A A,
     X = a X + B X.  Plain FP64 matrix products, no symmetry shortcut.
     With ``emulate_bf16`` the products are rounded to BF16 where the GPU
-    stores them (A, B, and each new X; the scale 1/s enters the first
-    step as on the GPU).  That mode is a diagnostic, not the reference.
+    stores them: A, then B' = aI + bA + cA^2 (the linear term folded into
+    the stored matrix), then each new X = B' X; the scale 1/s enters the
+    first step as on the GPU.  That mode is a diagnostic, not the
+    reference: both evaluation orders are the same polynomial.
     """
     X = np.asarray(X, dtype=np.float64)
     if X.shape[0] > X.shape[1]:
@@ -171,11 +173,12 @@ def newton_schulz(X: np.ndarray, s: float, steps: int = NS_STEPS,
     # Diagnostic path mirroring where the GPU rounds to BF16.
     Xk = X
     scale = 1.0 / s
+    eye = np.eye(X.shape[0])
     for k in range(steps):
         alpha = scale if k == 0 else 1.0
         A = _round_bf16_any((Xk @ Xk.T) * (alpha * alpha))
-        B = _round_bf16_any(b * A + c * (A @ A))
-        Xk = _round_bf16_any(alpha * (a * Xk + B @ Xk))
+        B = _round_bf16_any(a * eye + b * A + c * (A @ A))
+        Xk = _round_bf16_any(alpha * (B @ Xk))
     if steps == 0:
         Xk = _round_bf16_any(Xk * scale)
     return Xk

@@ -330,3 +330,13 @@ def test_closed_form_does_not_distinguish_gram_side():
     X = rng.standard_normal((5, 11))
     s = np.linalg.norm(X) + o.NORM_EPS
     assert rel(_mutant("gram_transposed")(X, s), closed_form(X, s)) < 1e-10
+
+
+def test_emulated_bf16_mode_is_close_to_exact():
+    # The diagnostic mode rounds where the GPU stores products; its error
+    # against the exact iteration is the BF16 floor the GPU tests allow for.
+    rng = np.random.default_rng(50)
+    X = o.bf16_rne(rng.standard_normal((64, 128)).astype(np.float32))
+    s = np.linalg.norm(X) + o.NORM_EPS
+    err = rel(o.newton_schulz(X, s, emulate_bf16=True), o.newton_schulz(X, s))
+    assert 1e-4 < err < 2e-2
