@@ -146,8 +146,20 @@ def frobenius_scale(M32: np.ndarray, eps: float = NORM_EPS) -> float:
 # ---------------------------------------------------------------------------
 # [DN] step 3, [XJ], [PT]: Newton-Schulz orthogonalisation of a whole matrix.
 # ---------------------------------------------------------------------------
+def step_coeffs(coeffs, steps: int) -> List[Tuple[float, float, float]]:
+    """Normalise ``coeffs`` to one (a, b, c) triple per step: a single
+    triple is used at every step; a sequence of ``steps`` triples is a
+    per-step schedule."""
+    c = list(coeffs)
+    if len(c) == 3 and not hasattr(c[0], "__len__"):
+        return [tuple(float(v) for v in c)] * steps
+    if len(c) != steps:
+        raise ValueError("a coefficient schedule needs one (a, b, c) per step")
+    return [tuple(float(v) for v in t) for t in c]
+
+
 def newton_schulz(X: np.ndarray, s: float, steps: int = NS_STEPS,
-                  coeffs: Sequence[float] = NS_COEFFS,
+                  coeffs: Sequence = NS_COEFFS,
                   emulate_bf16: bool = False) -> np.ndarray:
     """Quintic Newton-Schulz on a wide matrix X (rows <= cols).
 
@@ -162,10 +174,10 @@ def newton_schulz(X: np.ndarray, s: float, steps: int = NS_STEPS,
     X = np.asarray(X, dtype=np.float64)
     if X.shape[0] > X.shape[1]:
         raise ValueError("newton_schulz expects a wide matrix (rows <= cols)")
-    a, b, c = (float(v) for v in coeffs)
+    sched = step_coeffs(coeffs, steps)
     if not emulate_bf16:
         Xk = X / s
-        for _ in range(steps):
+        for a, b, c in sched:
             A = Xk @ Xk.T
             B = b * A + c * (A @ A)
             Xk = a * Xk + B @ Xk
@@ -174,7 +186,7 @@ def newton_schulz(X: np.ndarray, s: float, steps: int = NS_STEPS,
     Xk = X
     scale = 1.0 / s
     eye = np.eye(X.shape[0])
-    for k in range(steps):
+    for k, (a, b, c) in enumerate(sched):
         alpha = scale if k == 0 else 1.0
         A = _round_bf16_any((Xk @ Xk.T) * (alpha * alpha))
         B = _round_bf16_any(a * eye + b * A + c * (A @ A))
@@ -202,6 +214,36 @@ def apply_update(W: np.ndarray, O: np.ndarray, lr: float, wd: float,
     return out.astype(np.float32)
 
 
+# ---------------------------------------------------------------------------
+# Method variants (not on the pages; common Muon variants, exposed as
+# options).  Update scale rules multiply a group's own scale.
+# ---------------------------------------------------------------------------
+SCALE_NONE = 0          # 1
+SCALE_SQRT_ASPECT = 1   # sqrt(max(1, rows / cols))   (rows = output dim)
+SCALE_RMS_MATCH = 2     # rms_target * sqrt(max(rows, cols))
+
+
+def update_scale_rule(rule: int, rows: int, cols: int, rms_target: float = 0.2) -> float:
+    """Shape factor of the update for a weight of rows x cols, evaluated in
+    FP32 as the library does (sqrt of an FP32 ratio / size)."""
+    if rule == SCALE_NONE:
+        return 1.0
+    if rule == SCALE_SQRT_ASPECT:
+        r = np.float32(max(1.0, np.float32(rows) / np.float32(cols)))
+        return float(np.sqrt(r, dtype=np.float32))
+    if rule == SCALE_RMS_MATCH:
+        return float(np.float32(rms_target) * np.sqrt(np.float32(max(rows, cols)), dtype=np.float32))
+    raise ValueError(f"unknown scale rule {rule}")
+
+
+def nesterov_input(M_new: np.ndarray, G: np.ndarray, mu: float) -> np.ndarray:
+    """Nesterov variant: the matrix orthogonalised is G + mu*M' (FP64 sum,
+    stored as FP32), with M' the updated momentum."""
+    mu64 = as_f32_scalar(mu)
+    out = np.asarray(G, dtype=np.float64) + mu64 * np.asarray(M_new, dtype=np.float64)
+    return out.astype(np.float32)
+
+
 @dataclass
 class MatrixStep:
     """Everything the oracle computes for one matrix."""
@@ -216,16 +258,18 @@ class MatrixStep:
 def muon_step_matrix(W: np.ndarray, M: np.ndarray, G: np.ndarray, *,
                      lr: float, wd: float, mu: float,
                      ns_steps: int = NS_STEPS,
-                     coeffs: Sequence[float] = NS_COEFFS,
+                     coeffs: Sequence = NS_COEFFS,
                      eps: float = NORM_EPS, update_scale: float = 1.0,
-                     emulate_bf16: bool = False) -> MatrixStep:
+                     emulate_bf16: bool = False, nesterov: bool = False) -> MatrixStep:
     """The whole step for one matrix, in the pages' order ([DN] steps 1-5,
     without the two all-to-all exchanges, which move data but do not
-    change it)."""
+    change it).  With ``nesterov`` the orthogonalised matrix is G + mu*M'
+    instead of M'."""
     M_new = momentum_update(M, G, mu)                      # step 1
-    Xb = bf16_rne(M_new)                                   # step 1: cast
+    U = nesterov_input(M_new, G, mu) if nesterov else M_new
+    Xb = bf16_rne(U)                                       # step 1: cast
     Xw, transposed = to_wide(Xb)
-    s = frobenius_scale(M_new, eps)
+    s = frobenius_scale(U, eps)
     Ow = newton_schulz(Xw, s, ns_steps, coeffs, emulate_bf16)   # step 3
     O = Ow.T if transposed else Ow
     W_new = apply_update(W, O, lr, wd, update_scale)       # step 5

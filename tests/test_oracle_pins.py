@@ -340,3 +340,53 @@ def test_emulated_bf16_mode_is_close_to_exact():
     s = np.linalg.norm(X) + o.NORM_EPS
     err = rel(o.newton_schulz(X, s, emulate_bf16=True), o.newton_schulz(X, s))
     assert 1e-4 < err < 2e-2
+
+
+# --------------------------------------------------------------------------
+# Method variants
+# --------------------------------------------------------------------------
+def test_coefficient_schedule_closed_form():
+    rng = np.random.default_rng(60)
+    X = rng.standard_normal((9, 21))
+    s = np.linalg.norm(X) + o.NORM_EPS
+    sched = [(4.0, -5.0, 2.0), (3.4445, -4.7750, 2.0315), (2.5, -2.0, 0.6), (1.5, -0.5, 0.0)]
+    U, S, Vt = np.linalg.svd(X / s, full_matrices=False)
+    y = S.copy()
+    for a, b, c in sched:
+        y = a * y + b * y ** 3 + c * y ** 5
+    assert rel(o.newton_schulz(X, s, 4, sched), (U * y) @ Vt) < 1e-10
+    # A constant schedule equals the single-triple form.
+    const = [o.NS_COEFFS] * 5
+    assert rel(o.newton_schulz(X, s, 5, const), o.newton_schulz(X, s)) == 0.0
+    with pytest.raises(ValueError):
+        o.newton_schulz(X, s, 3, sched)
+
+
+def test_nesterov_hand_case():
+    M = np.array([[1.0, 2.0]], dtype=np.float32)
+    G = np.array([[0.5, -1.0]], dtype=np.float32)
+    M_new = o.momentum_update(M, G, 0.5)          # [1.0, 0.0]
+    assert o.nesterov_input(M_new, G, 0.5).tolist() == [[1.0, -1.0]]
+    # mu = 0: Nesterov and heavy ball both orthogonalise G.
+    rng = np.random.default_rng(61)
+    W, M, G = (rng.standard_normal((6, 10)).astype(np.float32) for _ in range(3))
+    a = o.muon_step_matrix(W, M, G, lr=0.02, wd=0.1, mu=0.0, nesterov=True)
+    b = o.muon_step_matrix(W, M, G, lr=0.02, wd=0.1, mu=0.0, nesterov=False)
+    np.testing.assert_array_equal(a.W_new, b.W_new)
+
+
+def test_nesterov_orthogonalises_g_plus_mu_m():
+    rng = np.random.default_rng(62)
+    W, M, G = (rng.standard_normal((8, 12)).astype(np.float32) for _ in range(3))
+    st = o.muon_step_matrix(W, M, G, lr=0.02, wd=0.1, mu=0.9, nesterov=True)
+    U = (G.astype(np.float64) + np.float64(np.float32(0.9)) * st.M_new.astype(np.float64)).astype(np.float32)
+    s = np.linalg.norm(U.astype(np.float64)) + o.NORM_EPS
+    assert rel(st.O, closed_form(o.bf16_rne(U), s)) < 1e-10
+
+
+@pytest.mark.parametrize("rows,cols,rule,want", [
+    (4096, 1536, o.SCALE_SQRT_ASPECT, np.sqrt(4096 / 1536)), (1536, 4096, o.SCALE_SQRT_ASPECT, 1.0),
+    (64, 64, o.SCALE_SQRT_ASPECT, 1.0), (1536, 4096, o.SCALE_RMS_MATCH, 0.2 * 64.0),
+    (100, 36, o.SCALE_RMS_MATCH, 0.2 * 10.0), (7, 5, o.SCALE_NONE, 1.0)])
+def test_update_scale_rules(rows, cols, rule, want):
+    assert abs(o.update_scale_rule(rule, rows, cols) - want) <= 1e-6 * want
