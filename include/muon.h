@@ -162,6 +162,35 @@ muon_status_t muon_step_host(muon_handle_t handle, const muon_group_t* groups, i
                              float* const* weights_host, float lr, float wd, float mu,
                              int32_t ns_steps, void* stream);
 
+/* Shape rules for the update scale (common Muon variants; the pages give
+ * no formula).  The factor multiplies each group's own update_scale. */
+typedef enum {
+  MUON_SCALE_NONE = 0,         /* 1 */
+  MUON_SCALE_SQRT_ASPECT = 1,  /* sqrt(max(1, rows / cols)), rows = output dim */
+  MUON_SCALE_RMS_MATCH = 2     /* rms_target * sqrt(max(rows, cols)) */
+} muon_scale_rule_t;
+
+/* Options of muon_step_ex. */
+typedef struct {
+  float lr, wd, mu;
+  int32_t ns_steps;       /* 0..64 */
+  int32_t nesterov;       /* 0: orthogonalise M' ; 1: orthogonalise G + mu*M' */
+  const float* coeffs;    /* host, NULL or 3*ns_steps floats: (a, b, c) per iteration */
+  int32_t scale_rule;     /* muon_scale_rule_t */
+  float rms_target;       /* MUON_SCALE_RMS_MATCH target (<= 0: 0.2) */
+} muon_options_t;
+
+/* muon_step with method variants: Nesterov momentum (the matrix
+ * orthogonalised, and normed, is U = G + mu*M' with M' the updated
+ * momentum), a per-iteration coefficient schedule, and a shape rule for
+ * the update scale.  With nesterov = 0, coeffs = NULL and
+ * MUON_SCALE_NONE it equals muon_step.  Same buffers and errors as
+ * muon_step; INVALID_ARG also for a NULL opts, an unknown rule or
+ * non-finite coefficients. */
+muon_status_t muon_step_ex(muon_handle_t handle, const muon_group_t* groups, int32_t n_groups,
+                           float* const* momentum_dev, const float* const* grad_dev,
+                           float* const* weights_dev, const muon_options_t* opts, void* stream);
+
 /* Step 1 alone: momentum update, BF16 cast into wide layout, and the
  * per-matrix inverse scale 1/(||M||_F + 1e-7).
  * momentum_dev:  count*rows*cols FP32, updated in place.
@@ -234,6 +263,15 @@ muon_status_t muon_newton_schulz_bf16_static(int32_t m, int32_t n, int32_t count
 /* Synchronise `stream`, then read and clear the handle's device error
  * flag: MUON_OK, MUON_ERR_TIMEOUT or MUON_ERR_NONFINITE. */
 muon_status_t muon_last_device_error(muon_handle_t handle, void* stream);
+
+/* Failure-path self-test of the bounded device waits: launches one small
+ * kernel that waits, through the same wait routine the Newton-Schulz
+ * kernels use, on a barrier nothing will complete.  The wait gives up after
+ * `limit_ms` (1..2000), sets the handle's device error flag and the kernel
+ * returns normally, leaving the context usable; muon_last_device_error()
+ * then reports MUON_ERR_TIMEOUT.  No fault, trap or hang is involved.
+ * Errors: INVALID_ARG (limit out of range), CUDA. */
+muon_status_t muon_selftest_bounded_wait(muon_handle_t handle, int32_t limit_ms, void* stream);
 
 /* Per-kernel timing: when enabled, every launch is bracketed by CUDA
  * events on the launching stream.  muon_kernel_stats synchronises the

@@ -10,16 +10,18 @@ from ._native import (  # noqa: F401
     EXPORTED, KERNEL_NAMES, LIB_PATH, Handle, MuonError, load_library, muon_apply_update,
     muon_create, muon_destroy, muon_kernel_stats, muon_last_device_error,
     muon_last_error_message, muon_momentum_cast, muon_newton_schulz_bf16, muon_newton_schulz_bf16_static,
-    muon_plan_describe,
+    muon_plan_describe, muon_selftest_bounded_wait,
     muon_reset_kernel_stats, muon_set_kernel_timing, muon_status_string, muon_step,
-    muon_step_host, muon_version,
+    muon_step_ex, muon_step_host, muon_version, SCALE_NONE, SCALE_SQRT_ASPECT, SCALE_RMS_MATCH,
 )
 
 __all__ = [
     "EXPORTED", "KERNEL_NAMES", "LIB_PATH", "Handle", "MuonError", "load_library",
     "muon_apply_update", "muon_create", "muon_destroy", "muon_kernel_stats",
     "muon_last_device_error", "muon_last_error_message", "muon_momentum_cast",
-    "muon_newton_schulz_bf16", "muon_newton_schulz_bf16_static", "muon_plan_describe", "muon_reset_kernel_stats",
-    "muon_set_kernel_timing", "muon_status_string", "muon_step", "muon_step_host",
+    "muon_newton_schulz_bf16", "muon_newton_schulz_bf16_static", "muon_plan_describe",
+    "muon_selftest_bounded_wait", "muon_reset_kernel_stats",
+    "muon_set_kernel_timing", "muon_status_string", "muon_step", "muon_step_ex", "muon_step_host",
+    "SCALE_NONE", "SCALE_SQRT_ASPECT", "SCALE_RMS_MATCH",
     "muon_version",
 ]

@@ -30,8 +30,9 @@ EXPORTED = (
     "muon_destroy", "muon_plan_describe", "muon_step", "muon_step_host", "muon_momentum_cast",
     "muon_newton_schulz_bf16", "muon_apply_update", "muon_last_device_error",
     "muon_set_kernel_timing", "muon_kernel_stats", "muon_reset_kernel_stats",
-    "muon_newton_schulz_bf16_static",
+    "muon_newton_schulz_bf16_static", "muon_selftest_bounded_wait", "muon_step_ex",
 )
+SCALE_NONE, SCALE_SQRT_ASPECT, SCALE_RMS_MATCH = 0, 1, 2
 
 
 class MuonError(RuntimeError):
@@ -50,6 +51,13 @@ class _Stats(ctypes.Structure):
     _fields_ = [("total_ms", ctypes.c_double * N_KERNELS),
                 ("launches", ctypes.c_int64 * N_KERNELS),
                 ("total_launches", ctypes.c_int64)]
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("wd", ctypes.c_float), ("mu", ctypes.c_float),
+                ("ns_steps", ctypes.c_int32), ("nesterov", ctypes.c_int32),
+                ("coeffs", ctypes.POINTER(ctypes.c_float)), ("scale_rule", ctypes.c_int32),
+                ("rms_target", ctypes.c_float)]
 
 
 class _PlanInfo(ctypes.Structure):
@@ -85,6 +93,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                               c_i32, c_vp]),
         "muon_step_host": (c_int, [c_vp, P(_Group), c_i32, P(c_vp), P(c_vp), P(c_vp), c_f, c_f,
                                    c_f, c_i32, c_vp]),
+        "muon_step_ex": (c_int, [c_vp, P(_Group), c_i32, P(c_vp), P(c_vp), P(c_vp), P(_Options),
+                                 c_vp]),
         "muon_momentum_cast": (c_int, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_f, c_vp, c_vp,
                                        c_vp]),
         "muon_newton_schulz_bf16": (c_int, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32,
@@ -94,6 +104,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "muon_newton_schulz_bf16_static": (c_int, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32,
                                                    P(c_f), c_vp, c_vp]),
         "muon_last_device_error": (c_int, [c_vp, c_vp]),
+        "muon_selftest_bounded_wait": (c_int, [c_vp, c_i32, c_vp]),
         "muon_set_kernel_timing": (c_int, [c_vp, c_i32]),
         "muon_kernel_stats": (c_int, [c_vp, P(_Stats)]),
         "muon_reset_kernel_stats": (c_int, [c_vp]),
@@ -199,6 +210,25 @@ def muon_step(handle: int, groups: Sequence[GroupLike], momentum: Sequence, grad
                                     _stream(stream)))
 
 
+def muon_step_ex(handle: int, groups: Sequence[GroupLike], momentum: Sequence, grad: Sequence,
+                 weights: Sequence, lr: float, wd: float, mu: float, ns_steps: int = 5,
+                 nesterov: bool = False, coeffs: Optional[Sequence] = None,
+                 scale_rule: int = SCALE_NONE, rms_target: float = 0.2, stream=None) -> None:
+    """muon_step with variants; ``coeffs`` is a list of ns_steps (a, b, c)."""
+    c = None
+    if coeffs is not None:
+        flat = [float(v) for t in coeffs for v in t]
+        if len(flat) != 3 * ns_steps:
+            raise ValueError("coeffs needs one (a, b, c) per iteration")
+        c = (ctypes.c_float * len(flat))(*flat)
+    opts = _Options(lr, wd, mu, ns_steps, 1 if nesterov else 0,
+                    ctypes.cast(c, ctypes.POINTER(ctypes.c_float)) if c is not None else None,
+                    scale_rule, rms_target)
+    _check(load_library().muon_step_ex(handle, _groups(groups), len(groups), _ptr_array(momentum),
+                                       _ptr_array(grad), _ptr_array(weights), ctypes.byref(opts),
+                                       _stream(stream)))
+
+
 def muon_step_host(handle: int, groups: Sequence[GroupLike], momentum: Sequence, grad: Sequence,
                    weights: Sequence, lr: float, wd: float, mu: float, ns_steps: int = 5,
                    stream=None) -> None:
@@ -246,6 +276,12 @@ def muon_apply_update(handle: int, rows: int, cols: int, count: int, weights, o_
 
 def muon_last_device_error(handle: int, stream=None) -> None:
     _check(load_library().muon_last_device_error(handle, _stream(stream)))
+
+
+def muon_selftest_bounded_wait(handle: int, limit_ms: int = 50, stream=None) -> None:
+    """Launch the bounded-wait self-test; muon_last_device_error then
+    raises MUON_ERR_TIMEOUT."""
+    _check(load_library().muon_selftest_bounded_wait(handle, limit_ms, _stream(stream)))
 
 
 def muon_set_kernel_timing(handle: int, enable: bool) -> None:

@@ -50,7 +50,9 @@ __device__ __forceinline__ Tv block_sum(Tv v, Tv* red) {
 }
 
 // grid = (tiles per matrix, count); tile = 64 source rows x 64 source cols.
-template <bool kTranspose>
+// With kNesterov the matrix cast (and normed) is U = G + mu * M' instead
+// of the updated momentum M' itself.
+template <bool kTranspose, bool kNesterov>
 __global__ void __launch_bounds__(kThreads) momentum_cast_kernel(
     int rows, int cols, float* __restrict__ M, const float* __restrict__ G, float mu,
     uint16_t* __restrict__ X, int64_t x_ld, int64_t x_ms, float* __restrict__ partials) {
@@ -86,14 +88,20 @@ __global__ void __launch_bounds__(kThreads) momentum_cast_kernel(
         m4.z = fmaf(mu, m4.z, g4.z);
         m4.w = fmaf(mu, m4.w, g4.w);
         *reinterpret_cast<float4*>(Mm + off) = m4;
-        v[0] = m4.x; v[1] = m4.y; v[2] = m4.z; v[3] = m4.w;
+        if constexpr (kNesterov) {
+          v[0] = fmaf(mu, m4.x, g4.x); v[1] = fmaf(mu, m4.y, g4.y);
+          v[2] = fmaf(mu, m4.z, g4.z); v[3] = fmaf(mu, m4.w, g4.w);
+        } else {
+          v[0] = m4.x; v[1] = m4.y; v[2] = m4.z; v[3] = m4.w;
+        }
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (c + e < cols) {
-            const float mv = fmaf(mu, Mm[off + e], Gm[off + e]);
+            const float gv = Gm[off + e];
+            const float mv = fmaf(mu, Mm[off + e], gv);
             Mm[off + e] = mv;
-            v[e] = mv;
+            v[e] = kNesterov ? fmaf(mu, mv, gv) : mv;
           }
         }
       }
@@ -256,15 +264,22 @@ __global__ void __launch_bounds__(kThreads) scale_bf16_kernel(
 
 cudaError_t launch_momentum_cast(int rows, int cols, int count, float* M, const float* G,
                                  float mu, uint16_t* X, int64_t x_ld, int64_t x_ms,
-                                 float* partials, cudaStream_t stream) {
+                                 float* partials, cudaStream_t stream, bool nesterov) {
   if (count <= 0) return cudaSuccess;
   const dim3 grid(ew_tiles_per_matrix(rows, cols), count);
-  if (rows > cols)
-    momentum_cast_kernel<true><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X, x_ld, x_ms,
-                                                              partials);
+  const bool tr = rows > cols;
+  if (tr && nesterov)
+    momentum_cast_kernel<true, true><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X, x_ld,
+                                                                    x_ms, partials);
+  else if (tr)
+    momentum_cast_kernel<true, false><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X,
+                                                                     x_ld, x_ms, partials);
+  else if (nesterov)
+    momentum_cast_kernel<false, true><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X,
+                                                                     x_ld, x_ms, partials);
   else
-    momentum_cast_kernel<false><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X, x_ld,
-                                                               x_ms, partials);
+    momentum_cast_kernel<false, false><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X,
+                                                                      x_ld, x_ms, partials);
   return cudaGetLastError();
 }
 

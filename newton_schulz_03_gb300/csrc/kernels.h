@@ -18,12 +18,13 @@ inline int ew_tiles_per_matrix(int rows, int cols) {
   return ((rows + kEwTile - 1) / kEwTile) * ((cols + kEwTile - 1) / kEwTile);
 }
 
-// Step 1: M <- mu*M + G (FP32, in place); X <- bf16_rne(M) in wide layout
-// (transposed when rows > cols) with row pitch x_ld and matrix pitch x_ms
-// (elements); partials[mat * tiles + tile] <- sum of M^2 over the tile.
+// Step 1: M <- mu*M + G (FP32, in place); U = M (or G + mu*M with
+// `nesterov`); X <- bf16_rne(U) in wide layout (transposed when
+// rows > cols) with row pitch x_ld and matrix pitch x_ms (elements);
+// partials[mat * tiles + tile] <- sum of U^2 over the tile.
 cudaError_t launch_momentum_cast(int rows, int cols, int count, float* M, const float* G,
                                  float mu, uint16_t* X, int64_t x_ld, int64_t x_ms,
-                                 float* partials, cudaStream_t stream);
+                                 float* partials, cudaStream_t stream, bool nesterov = false);
 
 // inv_norm[mat] <- 1 / (sqrt(sum of partials of mat) + eps); flags NaN/Inf.
 cudaError_t launch_norm_finalize(const float* partials, int per_matrix, int count, float eps,
@@ -65,6 +66,10 @@ cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float
 cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X,
                              BatchView X_out, const float* inv_norm, int* err, int grid_cap,
                              cudaStream_t stream);
+
+// One kernel whose barrier wait can never complete: the bounded wait must
+// expire after limit_ns and set kDevErrTimeout in *err.
+cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t stream);
 
 // Last error text of a tensor-map encode (host, thread-local).
 const char* ns_last_encode_error();

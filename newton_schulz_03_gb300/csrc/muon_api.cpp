@@ -291,10 +291,11 @@ struct Coeffs {
 
 // ns_steps iterations on `count` wide matrices.  Reads x (never written);
 // iteration k writes dst[k]; the last one lands in `out`.  A, B: scratch.
+// `sched` holds the (a, b, c) of every iteration (at least `steps` entries).
 muon_status_t run_newton_schulz(muon_handle_t h, int m, int n, int count, muon::BatchView x,
                                 muon::BatchView out, muon::BatchView other, muon::BatchView A,
-                                muon::BatchView B, const float* inv_norm, int steps, Coeffs co,
-                                cudaStream_t s) {
+                                muon::BatchView B, const float* inv_norm, int steps,
+                                const Coeffs* sched, cudaStream_t s) {
   if (steps == 0) {
     LaunchScope L(h, MUON_KERNEL_SCALE, s);
     cudaError_t e = muon::launch_scale_bf16(
@@ -309,6 +310,7 @@ muon_status_t run_newton_schulz(muon_handle_t h, int m, int n, int count, muon::
     const bool to_out = ((steps - 1 - k) % 2) == 0;
     muon::BatchView dst = to_out ? out : other;
     const float* inv = (k == 0) ? inv_norm : nullptr;
+    const Coeffs co = sched[k];
     cudaError_t e;
     {
       LaunchScope L(h, MUON_KERNEL_NS_GRAM, s);
@@ -472,12 +474,38 @@ muon_status_t muon_plan_describe(const muon_group_t* groups, int32_t n_groups, i
   return MUON_OK;
 }
 
-muon_status_t muon_step(muon_handle_t h, const muon_group_t* groups, int32_t n_groups,
+}  // extern "C"
+
+namespace {
+
+// Everything a step needs beyond the buffers.
+struct StepOptions {
+  float lr, wd, mu;
+  int32_t ns_steps;
+  bool nesterov = false;
+  std::vector<Coeffs> sched;  // one (a, b, c) per iteration
+  int32_t scale_rule = MUON_SCALE_NONE;
+  float rms_target = 0.2f;
+};
+
+// FP32 shape factor of a rule (sqrt of an FP32 ratio or size).
+float rule_scale(int32_t rule, int rows, int cols, float rms_target) {
+  switch (rule) {
+    case MUON_SCALE_SQRT_ASPECT:
+      return sqrtf(fmaxf(1.0f, static_cast<float>(rows) / static_cast<float>(cols)));
+    case MUON_SCALE_RMS_MATCH:
+      return rms_target * sqrtf(static_cast<float>(std::max(rows, cols)));
+    default:
+      return 1.0f;
+  }
+}
+
+muon_status_t step_impl(muon_handle_t h, const muon_group_t* groups, int32_t n_groups,
                         float* const* momentum, const float* const* grad, float* const* weights,
-                        float lr, float wd, float mu, int32_t ns_steps, void* stream) {
+                        const StepOptions& o, void* stream) {
   muon_status_t st = check_handle(h);
   if (st != MUON_OK) return st;
-  if (!finite3(lr, wd, mu)) return fail(MUON_ERR_INVALID_ARG, "lr, wd and mu must be finite");
+  if (!finite3(o.lr, o.wd, o.mu)) return fail(MUON_ERR_INVALID_ARG, "lr, wd and mu must be finite");
   st = validate_groups(groups, n_groups);
   if (st != MUON_OK) return st;
   if (n_groups > 0 && (momentum == nullptr || grad == nullptr || weights == nullptr))
@@ -489,6 +517,7 @@ muon_status_t muon_step(muon_handle_t h, const muon_group_t* groups, int32_t n_g
     if (!aligned16(momentum[g]) || !aligned16(grad[g]) || !aligned16(weights[g]))
       return fail(MUON_ERR_INVALID_ARG, "group %d: buffers must be 16-byte aligned", g);
   }
+  const int32_t ns_steps = o.ns_steps;
   const std::string key = plan_key_of(groups, n_groups, ns_steps);
   if (key != h->plan_key) {
     Plan P;
@@ -501,7 +530,6 @@ muon_status_t muon_step(muon_handle_t h, const muon_group_t* groups, int32_t n_g
   st = ensure_workspace(h, P.ws_bytes);
   if (st != MUON_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Coeffs co{MUON_NS_A, MUON_NS_B, MUON_NS_C};
   uint8_t* ws = static_cast<uint8_t*>(h->ws);
   for (const Chunk& c : P.chunks) {
     const ChunkLayout L = chunk_layout(c.m, c.n, c.count);
@@ -516,9 +544,9 @@ muon_status_t muon_step(muon_handle_t h, const muon_group_t* groups, int32_t n_g
       const muon_group_t& G = groups[sg.group];
       const int64_t off = sg.first * int64_t(G.rows) * G.cols;
       LaunchScope Ls(h, MUON_KERNEL_MOMENTUM_CAST, s);
-      cudaError_t e = muon::launch_momentum_cast(G.rows, G.cols, sg.count, momentum[sg.group] + off,
-                                                 grad[sg.group] + off, mu, x0 + sg.slot * xms,
-                                                 L.ldx, xms, part + int64_t(sg.slot) * L.tiles, s);
+      cudaError_t e = muon::launch_momentum_cast(
+          G.rows, G.cols, sg.count, momentum[sg.group] + off, grad[sg.group] + off, o.mu,
+          x0 + sg.slot * xms, L.ldx, xms, part + int64_t(sg.slot) * L.tiles, s, o.nesterov);
       if (e != cudaSuccess) return cuda_fail(e, "momentum_cast launch");
     }
     {
@@ -533,19 +561,67 @@ muon_status_t muon_step(muon_handle_t h, const muon_group_t* groups, int32_t n_g
     uint16_t* oth = (fin == x0) ? x1 : x0;
     const muon::BatchView vx0{x0, L.ldx, xms}, vfin{fin, L.ldx, xms}, voth{oth, L.ldx, xms};
     const muon::BatchView vA{A, L.ldm, ams}, vB{B, L.ldm, ams};
-    st = run_newton_schulz(h, c.m, c.n, c.count, vx0, vfin, voth, vA, vB, inv, ns_steps, co, s);
+    st = run_newton_schulz(h, c.m, c.n, c.count, vx0, vfin, voth, vA, vB, inv, ns_steps,
+                           o.sched.data(), s);
     if (st != MUON_OK) return st;
     for (const Segment& sg : c.segs) {
       const muon_group_t& G = groups[sg.group];
       const int64_t off = sg.first * int64_t(G.rows) * G.cols;
+      const float scale = G.update_scale * rule_scale(o.scale_rule, G.rows, G.cols, o.rms_target);
       LaunchScope Ls(h, MUON_KERNEL_APPLY, s);
       cudaError_t e = muon::launch_apply_update(G.rows, G.cols, sg.count, weights[sg.group] + off,
-                                                fin + sg.slot * xms, L.ldx, xms, lr, wd,
-                                                G.update_scale, s);
+                                                fin + sg.slot * xms, L.ldx, xms, o.lr, o.wd,
+                                                scale, s);
       if (e != cudaSuccess) return cuda_fail(e, "apply launch");
     }
   }
   return MUON_OK;
+}
+
+StepOptions default_options(float lr, float wd, float mu, int32_t ns_steps) {
+  StepOptions o;
+  o.lr = lr;
+  o.wd = wd;
+  o.mu = mu;
+  o.ns_steps = ns_steps;
+  o.sched.assign(ns_steps > 0 ? ns_steps : 1, Coeffs{MUON_NS_A, MUON_NS_B, MUON_NS_C});
+  return o;
+}
+
+}  // namespace
+
+extern "C" {
+
+muon_status_t muon_step(muon_handle_t h, const muon_group_t* groups, int32_t n_groups,
+                        float* const* momentum, const float* const* grad, float* const* weights,
+                        float lr, float wd, float mu, int32_t ns_steps, void* stream) {
+  if (ns_steps < 0 || ns_steps > kMaxSteps)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps out of range (%d)", ns_steps);
+  return step_impl(h, groups, n_groups, momentum, grad, weights,
+                   default_options(lr, wd, mu, ns_steps), stream);
+}
+
+muon_status_t muon_step_ex(muon_handle_t h, const muon_group_t* groups, int32_t n_groups,
+                           float* const* momentum, const float* const* grad,
+                           float* const* weights, const muon_options_t* opts, void* stream) {
+  if (opts == nullptr) return fail(MUON_ERR_INVALID_ARG, "opts is NULL");
+  if (opts->ns_steps < 0 || opts->ns_steps > kMaxSteps)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps out of range (%d)", opts->ns_steps);
+  if (opts->scale_rule < MUON_SCALE_NONE || opts->scale_rule > MUON_SCALE_RMS_MATCH)
+    return fail(MUON_ERR_INVALID_ARG, "unknown scale_rule %d", opts->scale_rule);
+  StepOptions o = default_options(opts->lr, opts->wd, opts->mu, opts->ns_steps);
+  o.nesterov = opts->nesterov != 0;
+  o.scale_rule = opts->scale_rule;
+  o.rms_target = opts->rms_target > 0.f ? opts->rms_target : 0.2f;
+  if (!std::isfinite(o.rms_target)) return fail(MUON_ERR_INVALID_ARG, "rms_target not finite");
+  if (opts->coeffs != nullptr) {
+    for (int k = 0; k < opts->ns_steps; ++k) {
+      const Coeffs c{opts->coeffs[3 * k], opts->coeffs[3 * k + 1], opts->coeffs[3 * k + 2]};
+      if (!finite3(c.a, c.b, c.c)) return fail(MUON_ERR_INVALID_ARG, "coefficient %d not finite", k);
+      o.sched[k] = c;
+    }
+  }
+  return step_impl(h, groups, n_groups, momentum, grad, weights, o, stream);
 }
 
 muon_status_t muon_step_host(muon_handle_t h, const muon_group_t* groups, int32_t n_groups,
@@ -722,6 +798,7 @@ muon_status_t muon_newton_schulz_bf16(muon_handle_t h, int32_t m, int32_t n, int
     co = Coeffs{coeffs[0], coeffs[1], coeffs[2]};
     if (!finite3(co.a, co.b, co.c)) return fail(MUON_ERR_INVALID_ARG, "coefficients not finite");
   }
+  const std::vector<Coeffs> sched(ns_steps > 0 ? ns_steps : 1, co);
   if (count == 0) return MUON_OK;
   if (x == nullptr || out == nullptr || inv_norm == nullptr)
     return fail(MUON_ERR_INVALID_ARG, "NULL buffer");
@@ -749,7 +826,8 @@ muon_status_t muon_newton_schulz_bf16(muon_handle_t h, int32_t m, int32_t n, int
     const int take = static_cast<int>(std::min<int64_t>(count - done, cap));
     const muon::BatchView vx{x + done * xms, n, xms}, vo{out + done * xms, n, xms};
     const muon::BatchView vt{other, n, xms}, vA{A, m, ams}, vB{B, m, ams};
-    st = run_newton_schulz(h, m, n, take, vx, vo, vt, vA, vB, inv_norm + done, ns_steps, co, s);
+    st = run_newton_schulz(h, m, n, take, vx, vo, vt, vA, vB, inv_norm + done, ns_steps,
+                           sched.data(), s);
     if (st != MUON_OK) return st;
   }
   return MUON_OK;
@@ -796,6 +874,17 @@ muon_status_t muon_last_device_error(muon_handle_t h, void* stream) {
   }
   if (flag & muon::kDevErrTimeout) return fail(MUON_ERR_TIMEOUT, "a device-side wait expired");
   if (flag & muon::kDevErrNonFinite) return fail(MUON_ERR_NONFINITE, "non-finite momentum norm");
+  return MUON_OK;
+}
+
+muon_status_t muon_selftest_bounded_wait(muon_handle_t h, int32_t limit_ms, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  if (limit_ms < 1 || limit_ms > 2000)
+    return fail(MUON_ERR_INVALID_ARG, "limit_ms must be in 1..2000 (got %d)", limit_ms);
+  cudaError_t e = muon::launch_bounded_wait_selftest(
+      h->dev_err, static_cast<uint64_t>(limit_ms) * 1000000ull, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return MUON_OK;
 }
 

@@ -59,7 +59,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 // Wait for the phase with the given parity to complete.  Returns false when
 // the time limit expires or *abort becomes non-zero.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort) {
+                                          const volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t addr = smem_addr(bar);
   if (mbar_try_wait(addr, parity)) return true;
   uint64_t t0 = globaltimer();
@@ -67,7 +68,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     if (mbar_try_wait(addr, parity)) return true;
     if ((i & 255u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }

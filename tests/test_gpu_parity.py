@@ -314,3 +314,36 @@ def test_step_host_pipeline_matches_device_step(ns, h):
         st = o.muon_step_matrix(W[i], M[i], G[i], lr=0.02, wd=0.1, mu=0.95)
         err = np.linalg.norm(Wh.numpy()[i].astype(np.float64) - st.W_new) / (0.02 * np.linalg.norm(st.O))
         assert err <= NS_TOL + 1e-3
+
+
+def test_bounded_wait_expires_and_context_survives(ns, h):
+    """A device wait that can never complete gives up after its limit,
+    reports MUON_ERR_TIMEOUT, and the context keeps working."""
+    import time
+    ns.muon_last_device_error(h)            # start clean
+    t0 = time.perf_counter()
+    ns.muon_selftest_bounded_wait(h, 50)
+    with pytest.raises(ns.MuonError) as ei:
+        ns.muon_last_device_error(h)
+    waited = time.perf_counter() - t0
+    assert ei.value.status_name == "MUON_ERR_TIMEOUT"
+    assert 0.04 <= waited < 5.0
+    ns.muon_last_device_error(h)            # cleared by the read
+    # The GPU still computes correctly afterwards.
+    m, n = 128, 256
+    rng = np.random.default_rng(8)
+    Xb = o.bf16_rne_bits(rng.standard_normal((1, m, n), dtype=np.float32))
+    Xf = o.bf16_bits_to_f64(Xb)
+    inv = np.array([1.0 / (np.linalg.norm(Xf[0]) + o.NORM_EPS)], dtype=np.float32)
+    out = torch.zeros((1, m, n), dtype=torch.int16, device="cuda")
+    ns.muon_newton_schulz_bf16(h, m, n, 1, dev(Xb.view(np.int16)), out, dev(inv), 5)
+    ns.muon_last_device_error(h)
+    got = o.bf16_bits_to_f64(u16(out))
+    assert rel_fro(got[0], o.newton_schulz(Xf[0], 1.0 / float(inv[0]))) <= NS_TOL
+
+
+def test_selftest_rejects_bad_limit(ns, h):
+    for bad in (0, 2001):
+        with pytest.raises(ns.MuonError) as ei:
+            ns.muon_selftest_bounded_wait(h, bad)
+        assert ei.value.status_name == "MUON_ERR_INVALID_ARG"
