@@ -304,11 +304,45 @@ def run_ours(args, world, rank, local):
     }
     if not args.skip_e2e:
         line["e2e"] = run_e2e(args, ns, h, w, groups, Ws, Ms, Gs, world)
+    if args.adamw:
+        line["adamw"] = run_adamw(ns, h, peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         del Ws, Ms, Gs
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     handle.close()
     return line
+
+
+def run_adamw(ns, h, hbm_peak):
+    """The AdamW companion on the non-Muon parameters of a rung-L=24 model
+    (untied input and output embeddings of 131072 x 2048, 49 norm vectors of
+    2048): 28 bytes per element (read p, g, m, v; write p, m, v)."""
+    import torch
+    sizes = [131072 * 2048, 131072 * 2048] + [2048] * 49
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(77)
+    P = [torch.randn(n, generator=gen, device="cuda") for n in sizes]
+    G = [torch.randn(n, generator=gen, device="cuda").mul_(1e-3) for n in sizes]
+    M = [torch.zeros(n, device="cuda") for n in sizes]
+    V = [torch.zeros(n, device="cuda") for n in sizes]
+    hp = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1)
+    for t in range(1, 4):
+        ns.muon_adamw_step(h, P, G, M, V, step=t, **hp)
+    ns.muon_reset_kernel_stats(h)
+    ns.muon_set_kernel_timing(h, True)
+    steps = 10
+    for t in range(4, 4 + steps):
+        ns.muon_adamw_step(h, P, G, M, V, step=t, **hp)
+    st = ns.muon_kernel_stats(h)
+    ns.muon_set_kernel_timing(h, False)
+    ns.muon_last_device_error(h)
+    n = sum(sizes)
+    ms = st["total_ms"]["adamw"] / steps
+    gbs = 28.0 * n / (ms / 1e3) / 1e9
+    return {"params": n, "ms_per_step": round(ms, 4), "achieved": round(gbs, 1), "unit": "GB/s",
+            "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "bound": "hbm",
+            "bytes_per_element": 28, "launches_per_step": st["launches"]["adamw"] / steps,
+            "workload": "rung L=24 non-Muon parameters: 2 x 131072x2048 embeddings + 49 x 2048 norms"}
 
 
 def dense_over_alg(w) -> float:
@@ -440,6 +474,8 @@ def main(argv=None):
     ap.add_argument("--max-count", type=int, default=0,
                     help="cap every group's matrix count (small profiling cases)")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--adamw", action="store_true",
+                    help="also measure the AdamW companion kernel (adds an 'adamw' object)")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

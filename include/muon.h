@@ -76,7 +76,8 @@ typedef enum {
   MUON_KERNEL_NS_UPDATE = 4,      /* X' = alpha (a X + B X) */
   MUON_KERNEL_APPLY = 5,          /* W = W (1 - lr wd) - lr s O */
   MUON_KERNEL_SCALE = 6,          /* ns_steps == 0: O = X / s */
-  MUON_KERNEL_COUNT = 7
+  MUON_KERNEL_ADAMW = 7,          /* AdamW companion */
+  MUON_KERNEL_COUNT = 8
 } muon_kernel_t;
 
 typedef struct {
@@ -263,6 +264,30 @@ muon_status_t muon_newton_schulz_bf16_static(int32_t m, int32_t n, int32_t count
 /* Synchronise `stream`, then read and clear the handle's device error
  * flag: MUON_OK, MUON_ERR_TIMEOUT or MUON_ERR_NONFINITE. */
 muon_status_t muon_last_device_error(muon_handle_t handle, void* stream);
+
+/* AdamW options (decoupled weight decay, bias correction; step >= 1 is the
+ * 1-based step count used for the bias corrections). */
+typedef struct {
+  float lr, beta1, beta2, eps, wd;
+  int32_t step;
+} muon_adamw_options_t;
+
+/* AdamW companion for the parameters Muon does not handle -- embeddings,
+ * norms, scalars ("Microsoft Reveals MAI-Base-2 Training Recipe", section
+ * "How to Make Parameter Updates Faster and More Stable?": Muon for 2-D
+ * non-embedding matrices, AdamW for the rest).  For every tensor i (FP32,
+ * numel[i] elements, device pointers, updated in place except grads):
+ *   p <- p (1 - lr wd);  m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g^2
+ *   p <- p - (lr / (1 - b1^step)) m / (sqrt(v) / sqrt(1 - b2^step) + eps)
+ * numel: host array; the four pointer arrays are host arrays of device
+ * pointers, 4-byte aligned (16-byte alignment enables vector access).
+ * Up to 40 tensors per kernel launch; more are launched in batches.
+ * Errors: INVALID_ARG (NULL, unaligned, beta outside [0,1), eps <= 0,
+ * step < 1, non-finite), CUDA. */
+muon_status_t muon_adamw_step(muon_handle_t handle, int32_t n_tensors, const int64_t* numel,
+                              float* const* params_dev, const float* const* grads_dev,
+                              float* const* exp_avg_dev, float* const* exp_avg_sq_dev,
+                              const muon_adamw_options_t* opts, void* stream);
 
 /* Failure-path self-test of the bounded device waits: launches one small
  * kernel that waits, through the same wait routine the Newton-Schulz

@@ -7,7 +7,8 @@ benchmark.
 """
 
 from ._native import (  # noqa: F401
-    EXPORTED, KERNEL_NAMES, LIB_PATH, Handle, MuonError, load_library, muon_apply_update,
+    EXPORTED, KERNEL_NAMES, LIB_PATH, Handle, MuonError, load_library, muon_adamw_step,
+    muon_apply_update,
     muon_create, muon_destroy, muon_kernel_stats, muon_last_device_error,
     muon_last_error_message, muon_momentum_cast, muon_newton_schulz_bf16, muon_newton_schulz_bf16_static,
     muon_plan_describe, muon_selftest_bounded_wait,
@@ -17,6 +18,7 @@ from ._native import (  # noqa: F401
 
 __all__ = [
     "EXPORTED", "KERNEL_NAMES", "LIB_PATH", "Handle", "MuonError", "load_library",
+    "muon_adamw_step",
     "muon_apply_update", "muon_create", "muon_destroy", "muon_kernel_stats",
     "muon_last_device_error", "muon_last_error_message", "muon_momentum_cast",
     "muon_newton_schulz_bf16", "muon_newton_schulz_bf16_static", "muon_plan_describe",

@@ -21,7 +21,8 @@ STATUS_NAMES = {
     4: "MUON_ERR_UNSUPPORTED_ARCH", 5: "MUON_ERR_TIMEOUT", 6: "MUON_ERR_NONFINITE",
     7: "MUON_ERR_NO_DEVICE",
 }
-KERNEL_NAMES = ("momentum_cast", "norm", "ns_gram", "ns_poly", "ns_update", "apply", "scale")
+KERNEL_NAMES = ("momentum_cast", "norm", "ns_gram", "ns_poly", "ns_update", "apply", "scale",
+                "adamw")
 N_KERNELS = len(KERNEL_NAMES)
 
 # Symbols the header declares (checked by the CPU test-suite).
@@ -31,6 +32,7 @@ EXPORTED = (
     "muon_newton_schulz_bf16", "muon_apply_update", "muon_last_device_error",
     "muon_set_kernel_timing", "muon_kernel_stats", "muon_reset_kernel_stats",
     "muon_newton_schulz_bf16_static", "muon_selftest_bounded_wait", "muon_step_ex",
+    "muon_adamw_step",
 )
 SCALE_NONE, SCALE_SQRT_ASPECT, SCALE_RMS_MATCH = 0, 1, 2
 
@@ -58,6 +60,11 @@ class _Options(ctypes.Structure):
                 ("ns_steps", ctypes.c_int32), ("nesterov", ctypes.c_int32),
                 ("coeffs", ctypes.POINTER(ctypes.c_float)), ("scale_rule", ctypes.c_int32),
                 ("rms_target", ctypes.c_float)]
+
+
+class _AdamwOptions(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("wd", ctypes.c_float), ("step", ctypes.c_int32)]
 
 
 class _PlanInfo(ctypes.Structure):
@@ -105,6 +112,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                                    P(c_f), c_vp, c_vp]),
         "muon_last_device_error": (c_int, [c_vp, c_vp]),
         "muon_selftest_bounded_wait": (c_int, [c_vp, c_i32, c_vp]),
+        "muon_adamw_step": (c_int, [c_vp, c_i32, P(ctypes.c_int64), P(c_vp), P(c_vp), P(c_vp),
+                                    P(c_vp), P(_AdamwOptions), c_vp]),
         "muon_set_kernel_timing": (c_int, [c_vp, c_i32]),
         "muon_kernel_stats": (c_int, [c_vp, P(_Stats)]),
         "muon_reset_kernel_stats": (c_int, [c_vp]),
@@ -276,6 +285,18 @@ def muon_apply_update(handle: int, rows: int, cols: int, count: int, weights, o_
 
 def muon_last_device_error(handle: int, stream=None) -> None:
     _check(load_library().muon_last_device_error(handle, _stream(stream)))
+
+
+def muon_adamw_step(handle: int, params: Sequence, grads: Sequence, exp_avg: Sequence,
+                    exp_avg_sq: Sequence, lr: float, beta1: float, beta2: float, eps: float,
+                    wd: float, step: int, stream=None) -> None:
+    """AdamW on FP32 tensors (updated in place); ``step`` is 1-based."""
+    n = len(params)
+    numel = (ctypes.c_int64 * max(n, 1))(*[int(t.numel()) for t in params])
+    opts = _AdamwOptions(lr, beta1, beta2, eps, wd, step)
+    _check(load_library().muon_adamw_step(handle, n, numel, _ptr_array(params), _ptr_array(grads),
+                                          _ptr_array(exp_avg), _ptr_array(exp_avg_sq),
+                                          ctypes.byref(opts), _stream(stream)))
 
 
 def muon_selftest_bounded_wait(handle: int, limit_ms: int = 50, stream=None) -> None:

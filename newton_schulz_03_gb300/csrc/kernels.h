@@ -67,6 +67,22 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X,
                              BatchView X_out, const float* inv_norm, int* err, int grid_cap,
                              cudaStream_t stream);
 
+// ------------------------------------------------------------------ AdamW
+constexpr int kAdamwMaxTensors = 40;
+// Tensors of one AdamW launch, passed by value in the kernel parameters.
+struct AdamwTable {
+  float* p[kAdamwMaxTensors];
+  const float* g[kAdamwMaxTensors];
+  float* m[kAdamwMaxTensors];
+  float* v[kAdamwMaxTensors];
+  int64_t n[kAdamwMaxTensors];
+  int64_t block_start[kAdamwMaxTensors + 1];  // prefix sum of blocks per tensor
+  int count;
+};
+int64_t adamw_blocks(int64_t numel);
+cudaError_t launch_adamw(const AdamwTable& table, float lr, float beta1, float beta2, float eps,
+                         float wd, int step, cudaStream_t stream);
+
 // One kernel whose barrier wait can never complete: the bounded wait must
 // expire after limit_ns and set kDevErrTimeout in *err.
 cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t stream);

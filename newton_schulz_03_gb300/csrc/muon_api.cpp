@@ -877,6 +877,61 @@ muon_status_t muon_last_device_error(muon_handle_t h, void* stream) {
   return MUON_OK;
 }
 
+muon_status_t muon_adamw_step(muon_handle_t h, int32_t n_tensors, const int64_t* numel,
+                              float* const* params, const float* const* grads,
+                              float* const* exp_avg, float* const* exp_avg_sq,
+                              const muon_adamw_options_t* opts, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  if (opts == nullptr) return fail(MUON_ERR_INVALID_ARG, "opts is NULL");
+  const muon_adamw_options_t& o = *opts;
+  if (!finite3(o.lr, o.wd, o.eps) || !finite3(o.beta1, o.beta2, 0.f))
+    return fail(MUON_ERR_INVALID_ARG, "AdamW scalars must be finite");
+  if (o.beta1 < 0.f || o.beta1 >= 1.f || o.beta2 < 0.f || o.beta2 >= 1.f || o.eps <= 0.f ||
+      o.step < 1)
+    return fail(MUON_ERR_INVALID_ARG, "need 0 <= beta < 1, eps > 0, step >= 1");
+  if (n_tensors < 0) return fail(MUON_ERR_INVALID_ARG, "n_tensors < 0");
+  if (n_tensors > 0 && (numel == nullptr || params == nullptr || grads == nullptr ||
+                        exp_avg == nullptr || exp_avg_sq == nullptr))
+    return fail(MUON_ERR_INVALID_ARG, "NULL array");
+  for (int i = 0; i < n_tensors; ++i) {
+    if (numel[i] < 0) return fail(MUON_ERR_INVALID_ARG, "tensor %d: numel < 0", i);
+    if (numel[i] == 0) continue;
+    const void* ptrs[4] = {params[i], grads[i], exp_avg[i], exp_avg_sq[i]};
+    for (const void* q : ptrs) {
+      if (q == nullptr) return fail(MUON_ERR_INVALID_ARG, "tensor %d: NULL buffer", i);
+      if (reinterpret_cast<uintptr_t>(q) & 3u)
+        return fail(MUON_ERR_INVALID_ARG, "tensor %d: buffers must be 4-byte aligned", i);
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  muon::AdamwTable table{};
+  auto flush = [&]() -> muon_status_t {
+    if (table.count == 0) return MUON_OK;
+    LaunchScope Ls(h, MUON_KERNEL_ADAMW, s);
+    cudaError_t e = muon::launch_adamw(table, o.lr, o.beta1, o.beta2, o.eps, o.wd, o.step, s);
+    table = muon::AdamwTable{};
+    if (e != cudaSuccess) return cuda_fail(e, "AdamW launch");
+    return MUON_OK;
+  };
+  for (int i = 0; i < n_tensors; ++i) {
+    if (numel[i] == 0) continue;
+    const int c = table.count;
+    table.p[c] = params[i];
+    table.g[c] = grads[i];
+    table.m[c] = exp_avg[i];
+    table.v[c] = exp_avg_sq[i];
+    table.n[c] = numel[i];
+    table.block_start[c + 1] = table.block_start[c] + muon::adamw_blocks(numel[i]);
+    table.count = c + 1;
+    if (table.count == muon::kAdamwMaxTensors || table.block_start[table.count] > (int64_t(1) << 30)) {
+      st = flush();
+      if (st != MUON_OK) return st;
+    }
+  }
+  return flush();
+}
+
 muon_status_t muon_selftest_bounded_wait(muon_handle_t h, int32_t limit_ms, void* stream) {
   muon_status_t st = check_handle(h);
   if (st != MUON_OK) return st;

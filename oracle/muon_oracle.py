@@ -322,3 +322,29 @@ def ns_algorithmic_flops(m: int, n: int, steps: int = NS_STEPS) -> int:
 def ns_dense_flops(m: int, n: int, steps: int = NS_STEPS) -> int:
     """Dense-equivalent flops per matrix (no symmetry): 5*(4 m^2 n + 2 m^3)."""
     return steps * (4 * m * m * n + 2 * m * m * m)
+
+
+# ---------------------------------------------------------------------------
+# AdamW companion for the parameters Muon does not handle (embeddings,
+# norms, scalars): "Microsoft Reveals MAI-Base-2 Training Recipe", section
+# "How to Make Parameter Updates Faster and More Stable?" (Muon for 2-D
+# non-embedding matrices, AdamW for the rest).  The pages give no formula;
+# this is the standard decoupled-decay AdamW with bias correction.
+# ---------------------------------------------------------------------------
+def adamw_step(p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.ndarray, *,
+               lr: float, beta1: float, beta2: float, eps: float, wd: float,
+               step: int):
+    """One AdamW step (step >= 1) in FP64 on FP32 inputs; returns the new
+    (p, m, v) as FP32.  p <- p (1 - lr wd); m <- b1 m + (1 - b1) g;
+    v <- b2 v + (1 - b2) g^2; p <- p - lr m_hat / (sqrt(v_hat) + eps) with
+    m_hat = m / (1 - b1^t), v_hat = v / (1 - b2^t)."""
+    lr, b1, b2 = as_f32_scalar(lr), as_f32_scalar(beta1), as_f32_scalar(beta2)
+    eps, wd = as_f32_scalar(eps), as_f32_scalar(wd)
+    p64 = np.asarray(p, np.float64) * (1.0 - lr * wd)
+    g64 = np.asarray(g, np.float64)
+    m64 = b1 * np.asarray(m, np.float64) + (1.0 - b1) * g64
+    v64 = b2 * np.asarray(v, np.float64) + (1.0 - b2) * g64 * g64
+    m_hat = m64 / (1.0 - b1 ** step)
+    v_hat = v64 / (1.0 - b2 ** step)
+    p64 = p64 - lr * m_hat / (np.sqrt(v_hat) + eps)
+    return p64.astype(np.float32), m64.astype(np.float32), v64.astype(np.float32)

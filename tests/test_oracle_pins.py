@@ -390,3 +390,40 @@ def test_nesterov_orthogonalises_g_plus_mu_m():
     (100, 36, o.SCALE_RMS_MATCH, 0.2 * 10.0), (7, 5, o.SCALE_NONE, 1.0)])
 def test_update_scale_rules(rows, cols, rule, want):
     assert abs(o.update_scale_rule(rule, rows, cols) - want) <= 1e-6 * want
+
+
+# --------------------------------------------------------------------------
+# AdamW companion
+# --------------------------------------------------------------------------
+def test_adamw_matches_torch_reference():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(70)
+    p0 = rng.standard_normal(1000).astype(np.float32)
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1)
+    p, m, v = p0.copy(), np.zeros_like(p0), np.zeros_like(p0)
+    tp = torch.nn.Parameter(torch.from_numpy(p0.astype(np.float64)))
+    f32 = o.as_f32_scalar
+    opt = torch.optim.AdamW([tp], lr=f32(hp["lr"]), betas=(f32(hp["beta1"]), f32(hp["beta2"])),
+                            eps=f32(hp["eps"]), weight_decay=f32(hp["wd"]), foreach=False)
+    for t in range(1, 6):
+        g = rng.standard_normal(1000).astype(np.float32)
+        p, m, v = o.adamw_step(p, g, m, v, step=t, **hp)
+        # The torch reference runs in FP64 on the same FP32 inputs each step.
+        tp.data = torch.from_numpy(p_prev.astype(np.float64)) if t > 1 else tp.data
+        tp.grad = torch.from_numpy(g.astype(np.float64))
+        opt.step()
+        p_prev = p
+        np.testing.assert_allclose(tp.data.numpy(), p.astype(np.float64), rtol=2e-7, atol=1e-9)
+
+
+def test_adamw_first_step_is_signed_lr():
+    # At t = 1 with zero state: m_hat = g, v_hat = g^2, so the update is
+    # lr * g / (|g| + eps) -- the sign of g times lr, minus decay.
+    g = np.array([2.0, -0.5, 1e-3], dtype=np.float32)
+    p = np.array([1.0, 1.0, 1.0], dtype=np.float32)
+    z = np.zeros(3, dtype=np.float32)
+    p1, m1, v1 = o.adamw_step(p, g, z, z, lr=0.01, beta1=0.9, beta2=0.99, eps=1e-12, wd=0.0,
+                              step=1)
+    np.testing.assert_allclose(p1, [0.99, 1.01, 0.99], rtol=1e-6)
+    np.testing.assert_allclose(m1, 0.1 * g, rtol=1e-6)
+    np.testing.assert_allclose(v1, 0.01 * g * g, rtol=1e-5)
