@@ -223,15 +223,30 @@ def run_ours(args, world, rank, local):
     plan = ns.muon_plan_describe(groups, w.ns_steps)
     layers = w.layers
 
-    def step():
+    def step_on(s):
         # One step of the workload: `layers` calls over the resident layer.
         for _ in range(layers):
-            ns.muon_step(h, groups, Ms, Gs, Ws, w.lr, w.wd, w.mu, w.ns_steps, stream)
+            ns.muon_step(h, groups, Ms, Gs, Ws, w.lr, w.wd, w.mu, w.ns_steps, s)
+
+    def step():
+        step_on(stream)
 
     sync = torch.cuda.synchronize
     step()
     ns.muon_last_device_error(h, stream)
     ns.muon_reset_kernel_stats(h)
+    graph_ms = None
+    if args.graph:
+        # The same step captured once in a CUDA graph and replayed.
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            step_on(cap)
+        stream.wait_stream(cap)
+        gsecs = timed_steps(g.replay, args.steps, args.warmup, world, stream, sync)
+        graph_ms = gsecs * 1e3 / args.steps
+        ns.muon_reset_kernel_stats(h)
 
     with ClockSampler(local) as clk:
         ns.muon_set_kernel_timing(h, True)
@@ -299,6 +314,7 @@ def run_ours(args, world, rank, local):
         "pct_of_bf16_peak": round(100 * tflops / peak, 2),
         "tflops_dense_equivalent": round(tflops * dense_over_alg(w), 1),
         "gpu_launches": gpu_launches,
+        "graph_replay_ms_per_step": round(graph_ms, 4) if graph_ms is not None else None,
         "clocks": clocks,
         "roofline": roofline,
     }
@@ -474,6 +490,8 @@ def main(argv=None):
     ap.add_argument("--max-count", type=int, default=0,
                     help="cap every group's matrix count (small profiling cases)")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph and replayed")
     ap.add_argument("--adamw", action="store_true",
                     help="also measure the AdamW companion kernel (adds an 'adamw' object)")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
