@@ -318,6 +318,29 @@ cudaError_t make_map(CUtensorMap* map, BatchView v, int cols, int rows, int coun
   return cudaSuccess;
 }
 
+// Output map for the TMA-store epilogue: 32 x 32 boxes, no swizzle (the
+// staging buffer is a dense 32 x 64-byte block).
+cudaError_t make_map_out(CUtensorMap* map, BatchView v, int cols, int rows, int count) {
+  EncodeFn enc = get_encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(count)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(v.ld) * 2,
+                                 static_cast<cuuint64_t>(v.ms) * 2};
+  const cuuint32_t box[3] = {32u, 32u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v.ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_encode_err, sizeof(g_encode_err), "output map encode failed (%d)",
+             static_cast<int>(r));
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 // 4-D view of a batch for MN-major operand tiles: (64 columns, rows,
 // 64-column chunks, matrix).  A box (64, 64, chunks, 1) lands in shared
 // memory as `chunks` consecutive 64 x 64 swizzled blocks -- the layout the
@@ -396,10 +419,11 @@ cudaError_t ns_gemm_init() {
 cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out,
                            const float* inv_norm, int* err, int grid_cap, cudaStream_t stream) {
   if (use_pairs(m)) {
-    CUtensorMap t128;
+    CUtensorMap t128, tout;
     cudaError_t e = make_map(&t128, X, n, m, count, kBM);
+    if (e == cudaSuccess) e = make_map_out(&tout, A_out, m, m, count);
     if (e != cudaSuccess) return e;
-    return ns_pair_gram(t128, m, n, count, A_out, inv_norm, err, grid_cap, stream);
+    return ns_pair_gram(t128, tout, m, n, count, A_out, inv_norm, err, grid_cap, stream);
   }
   // A-side rows in boxes of kBM, B-side rows in boxes of kSymBN.
   CUtensorMap tx, txb;
@@ -427,13 +451,15 @@ cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out
 cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float a, float b,
                            float c, int* err, int grid_cap, cudaStream_t stream) {
   if (use_pairs(m)) {
-    CUtensorMap t128, t64;
+    CUtensorMap t128, t64, tout;
     const int mn4d = (m % 64 == 0) ? 1 : 0;
     cudaError_t e = make_map(&t128, A, m, m, count, kBM);
     if (e == cudaSuccess)
       e = mn4d ? make_map_mn4d(&t64, A, m, m, count, 2) : make_map(&t64, A, m, m, count, kBK);
+    if (e == cudaSuccess) e = make_map_out(&tout, B_out, m, m, count);
     if (e != cudaSuccess) return e;
-    return ns_pair_poly(t128, t64, m, count, A, B_out, a, b, c, err, grid_cap, stream, mn4d);
+    return ns_pair_poly(t128, t64, tout, m, count, A, B_out, a, b, c, err, grid_cap, stream,
+                        mn4d);
   }
   CUtensorMap ta, tab;
   cudaError_t e = make_map(&ta, A, m, m, count, kBM);
@@ -471,7 +497,7 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, 
   e = make_map(&tx, X, n, m, count, kBK);
   if (e != cudaSuccess) return e;
   if (use_pairs(m)) {
-    CUtensorMap tb64, tx4;
+    CUtensorMap tb64, tx4, tout;
     const int mn4d = (m % 64 == 0 && n % 64 == 0) ? 1 : 0;
     if (mn4d) {
       e = make_map_mn4d(&tb64, B, m, m, count, 2);
@@ -480,8 +506,9 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, 
       e = make_map(&tb64, B, m, m, count, kBK);
       tx4 = tx;
     }
+    if (e == cudaSuccess) e = make_map_out(&tout, X_out, n, m, count);
     if (e != cudaSuccess) return e;
-    return ns_pair_update(tb, tb64, tx4, m, n, count, X_out, inv_norm, err, grid_cap, stream,
+    return ns_pair_update(tb, tb64, tx4, tout, m, n, count, X_out, inv_norm, err, grid_cap, stream,
                           mn4d);
   }
   NsArgs p{};

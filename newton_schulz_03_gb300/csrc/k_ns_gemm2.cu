@@ -52,10 +52,10 @@ constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB per CTA
 constexpr uint32_t kPairTxBytes = 2u * kStageBytes;
 constexpr int kStages = 6;
 constexpr int kTmemCols = 2 * kPairN;           // two 256-column accumulators
-// Slack after the last stage: keeps every operand read of the last stage
-// inside the allocation even for a descriptor that spans a full 256-row
-// operand.
+// After the operand ring: the epilogue's staging buffers (4 warps x 2 x
+// 2 KB, for TMA stores), inside a 32 KB region.
 constexpr int kTailPad = 32 * 1024;
+constexpr int kStageOutBytes = 4096;   // per epilogue warp
 constexpr int kSmemBytes = kStages * kStageBytes + kTailPad + 1024 + 256;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -64,7 +64,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_at,
                         const __grid_constant__ CUtensorMap tmap_b,
-                        const __grid_constant__ CUtensorMap tmap_bt, const NsArgs p) {
+                        const __grid_constant__ CUtensorMap tmap_bt,
+                        const __grid_constant__ CUtensorMap tmap_out, const NsArgs p) {
   // A-side operand: rows of X (GRAM), of A (POLY) or of B (UPDATE); A and B
   // are stored as upper 256-block triangles.  B-side operand: rows of X
   // (GRAM), of A (POLY), or X as an MN-major operand (UPDATE).
@@ -108,6 +109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tmap_b);
     if (kSymA) ptx::tma_prefetch_desc(&tmap_at);
     if (kSymB) ptx::tma_prefetch_desc(&tmap_bt);
+    ptx::tma_prefetch_desc(&tmap_out);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(tmem_holder, kTmemCols);
@@ -259,6 +261,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     const uint32_t empty_leader0 = ptx::mapa_shared(ptx::smem_addr(&tmem_empty[0]), 0);
     const uint32_t empty_leader1 = ptx::mapa_shared(ptx::smem_addr(&tmem_empty[1]), 0);
+    uint8_t* stage_out = smem + kStages * kStageBytes + (warp - 2) * kStageOutBytes;
+    int issued = 0;
     for (int t = pair; t < p.total_tiles; t += npairs) {
       int mat, ti, tj;
       decode_tile(p, MODE, kPairM, kPairN, t, mat, ti, tj);
@@ -279,14 +283,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float s = p.inv_norm[mat];
         alpha = (MODE == kGram) ? s * s : s;
       }
-      epilogue_tile<MODE, kPairN>(
-          p, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kPairN),
-          mat, rb * kBM + r_tile, aux, alpha);
+      epilogue_tile_tma<MODE, kPairN>(
+          p, &tmap_out,
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kPairN),
+          mat, rb * kBM + r_tile, rb * kBM + quad * 32, aux, alpha, stage_out, issued, lane);
       ptx::tc_fence_before();
       ptx::mbar_arrive_cluster(acc ? empty_leader1 : empty_leader0);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // All TMA stores of this warp complete before the CTA can exit.
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -326,14 +334,15 @@ int max_pairs() {
 
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tat, const CUtensorMap& tb,
-                        const CUtensorMap& tbt, const NsArgs& p, int grid_cap,
-                        cudaStream_t stream) {
+                        const CUtensorMap& tbt, const CUtensorMap& tout, const NsArgs& p,
+                        int grid_cap, cudaStream_t stream) {
   if (p.total_tiles <= 0) return cudaSuccess;
   int pairs = max_pairs<MODE>();
   if (pairs > grid_cap / 2) pairs = grid_cap / 2;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   if (pairs < 1) pairs = 1;
-  ns_gemm_pair_kernel<MODE><<<2 * pairs, kThreads, kSmemBytes, stream>>>(ta, tat, tb, tbt, p);
+  ns_gemm_pair_kernel<MODE><<<2 * pairs, kThreads, kSmemBytes, stream>>>(ta, tat, tb, tbt, tout,
+                                                                          p);
   return cudaGetLastError();
 }
 
@@ -347,7 +356,8 @@ cudaError_t ns_pair_init() {
   return cudaSuccess;
 }
 
-cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchView A_out,
+cudaError_t ns_pair_gram(const CUtensorMap& tx, const CUtensorMap& tout, int m, int n, int count,
+                         BatchView A_out,
                          const float* inv_norm, int* err, int grid_cap, cudaStream_t stream) {
   NsArgs p{};
   p.m = m;
@@ -363,12 +373,12 @@ cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchVi
   p.out_ms = A_out.ms;
   p.inv_norm = inv_norm;
   p.err = err;
-  return launch_pair<kGram>(tx, tx, tx, tx, p, grid_cap, stream);
+  return launch_pair<kGram>(tx, tx, tx, tx, tout, p, grid_cap, stream);
 }
 
-cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, int count,
-                         BatchView A, BatchView B_out, float a, float b, float c, int* err,
-                         int grid_cap, cudaStream_t stream, int mn4d) {
+cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, const CUtensorMap& tout,
+                         int m, int count, BatchView A, BatchView B_out, float a, float b, float c,
+                         int* err, int grid_cap, cudaStream_t stream, int mn4d) {
   NsArgs p{};
   p.mn4d = mn4d;
   p.m = m;
@@ -389,12 +399,13 @@ cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, 
   p.c1 = c;
   p.c2 = a;
   p.err = err;
-  return launch_pair<kPoly>(ta, ta_t, ta, ta_t, p, grid_cap, stream);
+  return launch_pair<kPoly>(ta, ta_t, ta, ta_t, tout, p, grid_cap, stream);
 }
 
 cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,
-                           int m, int n, int count, BatchView X_out, const float* inv_norm,
-                           int* err, int grid_cap, cudaStream_t stream, int mn4d) {
+                           const CUtensorMap& tout, int m, int n, int count, BatchView X_out,
+                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream,
+                           int mn4d) {
   NsArgs p{};
   p.mn4d = mn4d;
   p.m = m;
@@ -410,7 +421,7 @@ cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const
   p.out_ms = X_out.ms;
   p.inv_norm = inv_norm;
   p.err = err;
-  return launch_pair<kUpdate>(tb, tb_t, tx, tx, p, grid_cap, stream);
+  return launch_pair<kUpdate>(tb, tb_t, tx, tx, tout, p, grid_cap, stream);
 }
 
 }  // namespace muon

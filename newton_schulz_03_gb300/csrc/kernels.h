@@ -99,14 +99,16 @@ const char* ns_last_encode_error();
 #include <cuda.h>
 namespace muon {
 cudaError_t ns_pair_init();
-cudaError_t ns_pair_gram(const CUtensorMap& tx, int m, int n, int count, BatchView A_out,
-                         const float* inv_norm, int* err, int grid_cap, cudaStream_t stream);
-cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, int m, int count,
-                         BatchView A, BatchView B_out, float a, float b, float c, int* err,
-                         int grid_cap, cudaStream_t stream, int mn4d);
+cudaError_t ns_pair_gram(const CUtensorMap& tx, const CUtensorMap& tout, int m, int n, int count,
+                         BatchView A_out, const float* inv_norm, int* err, int grid_cap,
+                         cudaStream_t stream);
+cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, const CUtensorMap& tout,
+                         int m, int count, BatchView A, BatchView B_out, float a, float b, float c,
+                         int* err, int grid_cap, cudaStream_t stream, int mn4d);
 cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,
-                           int m, int n, int count, BatchView X_out, const float* inv_norm,
-                           int* err, int grid_cap, cudaStream_t stream, int mn4d);
+                           const CUtensorMap& tout, int m, int n, int count, BatchView X_out,
+                           const float* inv_norm, int* err, int grid_cap, cudaStream_t stream,
+                           int mn4d);
 
 // Record `msg` as the calling thread's last error text and return `status`
 // (read back through muon_last_error_message).

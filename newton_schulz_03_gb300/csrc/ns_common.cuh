@@ -4,6 +4,7 @@
 // symmetric products).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -193,6 +194,87 @@ __device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, i
           if (gcol0 + e < p.out_cols)
             o16[static_cast<int64_t>(gcol0 + e) * p.out_ld + grow] = to_bf16_bits(f[e]);
       }
+    }
+    aux.load(cb + kPre);
+  }
+  __syncwarp();
+}
+
+// Epilogue through shared memory and TMA stores (upper-triangle storage,
+// no mirror): each 32 x 32 chunk of this warp's rows is packed to BF16 in
+// a 2 KB staging buffer of the warp (two per warp, alternating) and
+// written by one TMA store, which also clips rows and columns past the
+// matrix.  `stage` is the warp's 4 KB staging area, `issued` its running
+// count of stores (for buffer reuse).  row0 is the warp's first row.
+template <int MODE, int BN>
+__device__ __forceinline__ void epilogue_tile_tma(const NsArgs& p, const CUtensorMap* tmap_out,
+                                                  uint32_t taddr, int mat, int grow, int row0,
+                                                  EpiAux<MODE, BN, false>& aux, float alpha,
+                                                  uint8_t* stage, int& issued, int lane) {
+  constexpr int kChunks = BN / 32;
+  constexpr int kPre = EpiAux<MODE, BN, false>::kPrefetch;
+  const bool warp_rows = row0 < p.m;   // some row of this warp is inside the matrix
+#pragma unroll
+  for (int cb = 0; cb < kChunks; ++cb) {
+    uint32_t v[32];
+    __syncwarp();
+    ptx::tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cb * 32), v);
+    ptx::tmem_ld_wait();
+    const int gcol0 = aux.col0 + cb * 32;
+    if (warp_rows && gcol0 < p.out_cols) {
+      float f[32];
+      if (MODE != kPoly) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = alpha * __uint_as_float(v[e]);
+      } else {
+        float x[32];
+        if (aux.live(cb) && aux.full(cb)) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 u = aux.pre[cb % kPre][q];
+            x[q * 8 + 0] = bf16lo(u.x); x[q * 8 + 1] = bf16hi(u.x);
+            x[q * 8 + 2] = bf16lo(u.y); x[q * 8 + 3] = bf16hi(u.y);
+            x[q * 8 + 4] = bf16lo(u.z); x[q * 8 + 5] = bf16hi(u.z);
+            x[q * 8 + 6] = bf16lo(u.w); x[q * 8 + 7] = bf16hi(u.w);
+          }
+        } else {
+          const uint16_t* a16 = reinterpret_cast<const uint16_t*>(aux.row + gcol0);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            x[e] = (aux.row_ok && gcol0 + e < p.out_cols)
+                       ? __uint_as_float(static_cast<uint32_t>(a16[e]) << 16)
+                       : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float d = (gcol0 + e == grow) ? p.c2 : 0.f;
+          f[e] = fmaf(p.c1, __uint_as_float(v[e]), fmaf(p.c0, x[e], d));
+        }
+      }
+      // Reuse a staging buffer only after the store issued from it two
+      // stores ago has finished reading shared memory.
+      uint8_t* buf = stage + (issued & 1) * 2048;
+      if (issued >= 2) {
+        if (lane == 0) ptx::bulk_wait_read<1>();
+        __syncwarp();
+      }
+      uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        u.x = pack_bf16(f[q * 8 + 0], f[q * 8 + 1]);
+        u.y = pack_bf16(f[q * 8 + 2], f[q * 8 + 3]);
+        u.z = pack_bf16(f[q * 8 + 4], f[q * 8 + 5]);
+        u.w = pack_bf16(f[q * 8 + 6], f[q * 8 + 7]);
+        dst[q] = u;
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_3d(tmap_out, buf, gcol0, row0, mat);
+        ptx::bulk_commit();
+      }
+      ++issued;
     }
     aux.load(cb + kPre);
   }

@@ -347,3 +347,27 @@ def test_selftest_rejects_bad_limit(ns, h):
         with pytest.raises(ns.MuonError) as ei:
             ns.muon_selftest_bounded_wait(h, bad)
         assert ei.value.status_name == "MUON_ERR_INVALID_ARG"
+
+
+@pytest.mark.parametrize("rows,cols,count", [(256, 512, 2), (512, 256, 2), (200, 136, 1),
+                                             (2048, 1536, 1)])
+def test_step_equals_separate_entry_points(ns, h, rows, cols, count):
+    """muon_step equals momentum_cast -> newton_schulz_bf16 ->
+    apply_update called one after another, bit for bit (per-matrix results
+    do not depend on how matrices are batched or padded)."""
+    rng = np.random.default_rng(rows + cols)
+    W, M, G = (rng.standard_normal((count, rows, cols), dtype=np.float32) for _ in range(3))
+    lr, wd, mu = 0.02, 0.1, 0.95
+    dW, dM, dG = dev(W), dev(M), dev(G)
+    ns.muon_step(h, [(rows, cols, count)], [dM], [dG], [dW], lr, wd, mu, 5)
+    m, n = min(rows, cols), max(rows, cols)
+    sW, sM, sG = dev(W), dev(M), dev(G)
+    X = torch.zeros((count, m, n), dtype=torch.int16, device="cuda")
+    O = torch.zeros((count, m, n), dtype=torch.int16, device="cuda")
+    inv = torch.zeros(count, dtype=torch.float32, device="cuda")
+    ns.muon_momentum_cast(h, rows, cols, count, sM, sG, mu, X, inv)
+    ns.muon_newton_schulz_bf16(h, m, n, count, X, O, inv, 5)
+    ns.muon_apply_update(h, rows, cols, count, sW, O, lr, wd, 1.0)
+    ns.muon_last_device_error(h)
+    assert torch.equal(dM, sM)
+    assert torch.equal(dW, sW)
