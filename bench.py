@@ -37,7 +37,8 @@ UNIT = "matrices/s"
 DEFAULT_WORKLOAD = "l24_attention"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DOMINANT = "ns_update"
-NS_SOURCES = ("newton_schulz_03_gb300/csrc/k_ns_gemm.cu", "newton_schulz_03_gb300/csrc/sm103_ptx.cuh")
+NS_SOURCES = ("newton_schulz_03_gb300/csrc/k_ns_gemm.cu", "newton_schulz_03_gb300/csrc/k_ns_gemm2.cu",
+              "newton_schulz_03_gb300/csrc/ns_common.cuh", "newton_schulz_03_gb300/csrc/sm103_ptx.cuh")
 
 
 # ----------------------------------------------------------------- harness
@@ -169,9 +170,11 @@ def ns_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, matrices_per_launch: float):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    summary, if it was taken on the current kernel source.  The summary gives
+    bytes per matrix (traffic grows with the matrix count); one launch covers
+    ``matrices_per_launch`` matrices on average."""
     path = os.path.join(ROOT, "profiles", f"{DOMINANT}_{workload.split('[')[0]}.txt")
     if not os.path.exists(path):
         return None
@@ -183,7 +186,7 @@ def profiled_traffic(workload: str):
     if kv.get("kernel_source_sha256_16") != ns_source_hash():
         return None
     try:
-        return float(kv["dram_bytes_per_launch"])
+        return round(float(kv["dram_bytes_per_matrix"]) * matrices_per_launch)
     except (KeyError, ValueError):
         return None
 
@@ -281,9 +284,12 @@ def run_ours(args, world, rank, local):
     ns_tflops = (flops_step * steps_recorded) / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
     kernel_share = {k: round(v / max(sum(stats["total_ms"].values()), 1e-9), 4)
                     for k, v in stats["total_ms"].items() if v > 0}
-    traffic = profiled_traffic(w.name)
+    upd_matrices_step = sum(w.wide_batches().values()) * w.ns_steps * layers
+    traffic = profiled_traffic(w.name, upd_matrices_step * steps_recorded / upd_launches) \
+        if upd_launches else None
     roofline = {
-        "kernel": "ns_gemm_kernel<update,256> (X' = a X + B X)",
+        "kernel": ("ns_gemm_pair_kernel<update>" if min(m for m, _ in w.wide_batches()) > 128
+                   else "ns_gemm_kernel<update,256>") + " (X' = alpha B' X)",
         "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
         "peak": peak, "unit": "TFLOP/s",
         "frac": round(achieved / peak, 4) if achieved else None,
