@@ -252,17 +252,24 @@ def run_ours(args, world, rank, local):
         ns.muon_reset_kernel_stats(h)
 
     with ClockSampler(local) as clk:
-        ns.muon_set_kernel_timing(h, True)
+        # The step as a user runs it: no per-kernel events.
         ns.muon_reset_kernel_stats(h)
         launches0 = ns.muon_kernel_stats(h)["total_launches"]
         secs = timed_steps(step, args.steps, args.warmup, world, stream, sync)
+        launches1 = ns.muon_kernel_stats(h)["total_launches"]
+        # The same K steps again with an event pair around every launch on
+        # the launching stream: per-kernel durations for the roofline.  The
+        # events serialise the launches, so this pass is a little slower.
+        ns.muon_set_kernel_timing(h, True)
+        ns.muon_reset_kernel_stats(h)
+        secs_ev = timed_steps(step, args.steps, args.warmup, world, stream, sync)
         stats = ns.muon_kernel_stats(h)
         ns.muon_set_kernel_timing(h, False)
     ns.muon_last_device_error(h, stream)
     clocks = clk.summary()
     # Launch and time counts include the warm-up steps; scale to the timed K.
     frac_timed = args.steps / float(args.steps + args.warmup)
-    gpu_launches = int(round((stats["total_launches"] - launches0) * frac_timed))
+    gpu_launches = int(round((launches1 - launches0) * frac_timed))
 
     matrices_per_step = w.matrices
     value = job_value(world, matrices_per_step, args.steps, secs)
@@ -321,6 +328,8 @@ def run_ours(args, world, rank, local):
         "tflops_dense_equivalent": round(tflops * dense_over_alg(w), 1),
         "gpu_launches": gpu_launches,
         "graph_replay_ms_per_step": round(graph_ms, 4) if graph_ms is not None else None,
+        "ms_per_step_with_kernel_events": round(secs_ev * 1e3 / args.steps, 4),
+        "programmatic_dependent_launch": os.environ.get("MUON_PDL", "1") != "0",
         "clocks": clocks,
         "roofline": roofline,
     }

@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace muon {
 namespace {
@@ -56,6 +57,8 @@ template <bool kTranspose, bool kNesterov>
 __global__ void __launch_bounds__(kThreads) momentum_cast_kernel(
     int rows, int cols, float* __restrict__ M, const float* __restrict__ G, float mu,
     uint16_t* __restrict__ X, int64_t x_ld, int64_t x_ms, float* __restrict__ partials) {
+  grid_dep_wait();    // inputs come from the previous kernel of the step
+  grid_dep_launch();
   __shared__ __align__(16) uint16_t sT[kTranspose ? T : 1][T + kPad];
   __shared__ float red[kThreads / 32];
 
@@ -155,6 +158,8 @@ __global__ void __launch_bounds__(kThreads) momentum_cast_kernel(
 __global__ void __launch_bounds__(kThreads) norm_finalize_kernel(
     const float* __restrict__ partials, int per_matrix, float eps, float* __restrict__ inv_norm,
     int* __restrict__ err) {
+  grid_dep_wait();    // inputs come from the previous kernel of the step
+  grid_dep_launch();
   __shared__ double red[kThreads / 32];
   const int64_t mat = blockIdx.x;
   const float* p = partials + mat * per_matrix;
@@ -176,6 +181,8 @@ template <bool kTranspose>
 __global__ void __launch_bounds__(kThreads) apply_update_kernel(
     int rows, int cols, float* __restrict__ W, const uint16_t* __restrict__ O, int64_t o_ld,
     int64_t o_ms, float lr, float wd, float scale) {
+  grid_dep_wait();    // inputs come from the previous kernel of the step
+  grid_dep_launch();
   __shared__ __align__(16) uint16_t sO[kTranspose ? T : 1][T + kPad];
   const int tiles_c = (cols + T - 1) / T;
   const int tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
@@ -249,6 +256,8 @@ __global__ void __launch_bounds__(kThreads) apply_update_kernel(
 __global__ void __launch_bounds__(kThreads) scale_bf16_kernel(
     int m, int n, const uint16_t* __restrict__ x, int64_t x_ld, int64_t x_ms,
     uint16_t* __restrict__ out, int64_t o_ld, int64_t o_ms, const float* __restrict__ inv_norm) {
+  grid_dep_wait();    // inputs come from the previous kernel of the step
+  grid_dep_launch();
   const int64_t mat = blockIdx.y;
   const float s = inv_norm[mat];
   const int64_t total = static_cast<int64_t>(m) * n;
@@ -267,27 +276,18 @@ cudaError_t launch_momentum_cast(int rows, int cols, int count, float* M, const 
                                  float* partials, cudaStream_t stream, bool nesterov) {
   if (count <= 0) return cudaSuccess;
   const dim3 grid(ew_tiles_per_matrix(rows, cols), count);
+  const dim3 block(kThreads);
   const bool tr = rows > cols;
-  if (tr && nesterov)
-    momentum_cast_kernel<true, true><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X, x_ld,
-                                                                    x_ms, partials);
-  else if (tr)
-    momentum_cast_kernel<true, false><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X,
-                                                                     x_ld, x_ms, partials);
-  else if (nesterov)
-    momentum_cast_kernel<false, true><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X,
-                                                                     x_ld, x_ms, partials);
-  else
-    momentum_cast_kernel<false, false><<<grid, kThreads, 0, stream>>>(rows, cols, M, G, mu, X,
-                                                                      x_ld, x_ms, partials);
-  return cudaGetLastError();
+  auto kern = tr ? (nesterov ? momentum_cast_kernel<true, true> : momentum_cast_kernel<true, false>)
+                 : (nesterov ? momentum_cast_kernel<false, true> : momentum_cast_kernel<false, false>);
+  return launch_pdl(kern, grid, block, 0, stream, rows, cols, M, G, mu, X, x_ld, x_ms, partials);
 }
 
 cudaError_t launch_norm_finalize(const float* partials, int per_matrix, int count, float eps,
                                  float* inv_norm, int* err, cudaStream_t stream) {
   if (count <= 0) return cudaSuccess;
-  norm_finalize_kernel<<<count, kThreads, 0, stream>>>(partials, per_matrix, eps, inv_norm, err);
-  return cudaGetLastError();
+  return launch_pdl(norm_finalize_kernel, dim3(count), dim3(kThreads), 0, stream, partials,
+                    per_matrix, eps, inv_norm, err);
 }
 
 cudaError_t launch_apply_update(int rows, int cols, int count, float* W, const uint16_t* O,
@@ -295,13 +295,9 @@ cudaError_t launch_apply_update(int rows, int cols, int count, float* W, const u
                                 cudaStream_t stream) {
   if (count <= 0) return cudaSuccess;
   const dim3 grid(ew_tiles_per_matrix(rows, cols), count);
-  if (rows > cols)
-    apply_update_kernel<true><<<grid, kThreads, 0, stream>>>(rows, cols, W, O, o_ld, o_ms, lr, wd,
-                                                             scale);
-  else
-    apply_update_kernel<false><<<grid, kThreads, 0, stream>>>(rows, cols, W, O, o_ld, o_ms, lr,
-                                                              wd, scale);
-  return cudaGetLastError();
+  auto kern = rows > cols ? apply_update_kernel<true> : apply_update_kernel<false>;
+  return launch_pdl(kern, grid, dim3(kThreads), 0, stream, rows, cols, W, O, o_ld, o_ms, lr, wd,
+                    scale);
 }
 
 cudaError_t launch_scale_bf16(int m, int n, int count, const uint16_t* x, int64_t x_ld,
@@ -312,8 +308,8 @@ cudaError_t launch_scale_bf16(int m, int n, int count, const uint16_t* x, int64_
   int64_t blocks = (total + kThreads - 1) / kThreads;
   if (blocks > 4096) blocks = 4096;
   const dim3 grid(static_cast<unsigned>(blocks), count);
-  scale_bf16_kernel<<<grid, kThreads, 0, stream>>>(m, n, x, x_ld, x_ms, out, o_ld, o_ms, inv_norm);
-  return cudaGetLastError();
+  return launch_pdl(scale_bf16_kernel, grid, dim3(kThreads), 0, stream, m, n, x, x_ld, x_ms, out,
+                    o_ld, o_ms, inv_norm);
 }
 
 }  // namespace muon

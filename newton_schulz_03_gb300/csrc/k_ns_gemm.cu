@@ -42,6 +42,7 @@
 #include <cstring>
 
 #include "kernels.h"
+#include "launch.cuh"
 #include "ns_common.cuh"
 #include "sm103_ptx.cuh"
 
@@ -110,6 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Set-up above overlaps the previous kernel's tail; its outputs are read
+  // only from here on.
+  grid_dep_wait();
+  grid_dep_launch();
 
   const int num_kb = (p.K + kBK - 1) / kBK;
 
@@ -371,8 +376,8 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const NsArgs& p
                    cudaStream_t stream) {
   if (p.total_tiles <= 0) return cudaSuccess;
   const int grid = p.total_tiles < grid_cap ? p.total_tiles : grid_cap;
-  ns_gemm_kernel<MODE, BN><<<grid, kThreads, TileCfg<BN>::kSmemBytes, stream>>>(ta, tb, p);
-  return cudaGetLastError();
+  return launch_pdl(ns_gemm_kernel<MODE, BN>, dim3(grid), dim3(kThreads), TileCfg<BN>::kSmemBytes,
+                    stream, ta, tb, p);
 }
 
 template <int MODE, int BN>

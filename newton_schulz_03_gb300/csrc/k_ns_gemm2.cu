@@ -33,6 +33,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "launch.cuh"
 #include "ns_common.cuh"
 #include "sm103_ptx.cuh"
 
@@ -120,6 +121,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();  // barriers of both CTAs initialised before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Set-up above overlaps the previous kernel's tail; its outputs are read
+  // only from here on.
+  grid_dep_wait();
+  grid_dep_launch();
   const int num_kb = (p.K + kBK - 1) / kBK;
 
   if (warp == 0) {
@@ -341,9 +346,8 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tat, const CUt
   if (pairs > grid_cap / 2) pairs = grid_cap / 2;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   if (pairs < 1) pairs = 1;
-  ns_gemm_pair_kernel<MODE><<<2 * pairs, kThreads, kSmemBytes, stream>>>(ta, tat, tb, tbt, tout,
-                                                                          p);
-  return cudaGetLastError();
+  return launch_pdl(ns_gemm_pair_kernel<MODE>, dim3(2 * pairs), dim3(kThreads), kSmemBytes, stream,
+                    ta, tat, tb, tbt, tout, p);
 }
 
 }  // namespace

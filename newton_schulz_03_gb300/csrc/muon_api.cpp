@@ -667,6 +667,44 @@ muon_status_t muon_step_host(muon_handle_t h, const muon_group_t* groups, int32_
     }
   }
   if (pieces.empty()) return MUON_OK;
+  // Nothing overlaps the first piece's copy in or the last piece's copy
+  // out: split those two into pieces of 1, 2, 4, ... units so that the
+  // pipeline fills and drains with small copies.
+  {
+    // Smallest ramp piece: 16 MB of state or one matrix.
+    auto ramp = [groups](const Piece& p, bool up) {
+      std::vector<Piece> out;
+      int left = p.count;
+      const int64_t per = int64_t(groups[p.group].rows) * groups[p.group].cols;
+      const int unit = static_cast<int>(
+          std::max<int64_t>(1, static_cast<int64_t>((size_t(16) << 20) / (12 * size_t(per)))));
+      std::vector<int> sizes;
+      for (int s = unit; left > 0; s *= 2) {
+        const int take = std::min(s, left);
+        sizes.push_back(take);
+        left -= take;
+        if (2 * s >= left) {        // the rest in one piece (never above the original)
+          if (left > 0) sizes.push_back(left);
+          break;
+        }
+      }
+      if (!up) std::reverse(sizes.begin(), sizes.end());
+      int64_t first = p.first;
+      for (int s : sizes) {
+        out.push_back({p.group, first, s});
+        first += s;
+      }
+      return out;
+    };
+    std::vector<Piece> head = ramp(pieces.front(), true);
+    std::vector<Piece> rebuilt(head.begin(), head.end());
+    if (pieces.size() > 1) {
+      rebuilt.insert(rebuilt.end(), pieces.begin() + 1, pieces.end() - 1);
+      std::vector<Piece> tail = ramp(pieces.back(), false);
+      rebuilt.insert(rebuilt.end(), tail.begin(), tail.end());
+    }
+    pieces.swap(rebuilt);
+  }
 
   const size_t bytes = size_t(kSlots) * 3 * slot_elems * sizeof(float);
   if (h->staging_bytes < bytes) {
