@@ -1,0 +1,113 @@
+"""Extreme sizes through muon_step, checked against the CPU oracle:
+
+* one matrix of more than 2^31 elements (65536 x 40000, tall, so it also
+  runs through the transposing kernels) whose only non-zero entries form a
+  small block near its far corner.  Zero padding is exact for the method
+  (the norm, A = X X^T, the polynomial and the update all keep the zeros),
+  so the step must leave every entry outside the block exactly zero and
+  give the oracle's step of the block inside it.  Every flat offset of the
+  block is above 2^31, so 32-bit index arithmetic anywhere shows up;
+* the largest accepted dimension, 2^20, as the long side of wide and tall
+  matrices (K = 2^20 in the Gram product), on both Newton-Schulz kernels;
+* a group of more matrices than one elementwise launch covers (65535).
+"""
+
+import numpy as np
+import pytest
+
+from oracle import muon_oracle as o
+from tests.gpu_helpers import ulp_close
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+LR, WD, MU, STEPS = 0.02, 0.1, 0.95, 5
+
+
+@pytest.fixture(scope="module")
+def ns():
+    from newton_schulz_03_gb300 import build_lib
+    build_lib.build()
+    import newton_schulz_03_gb300 as pkg
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def h(ns):
+    handle = ns.Handle()
+    yield handle.value
+    handle.close()
+
+
+def update_error(Wg, st, W0):
+    """Relative error of the applied update against the oracle's step."""
+    on = np.linalg.norm(st.O)
+    dw = np.linalg.norm(Wg.astype(np.float64) - st.W_new.astype(np.float64))
+    fp = 1e-6 * (np.linalg.norm(W0) + LR * on)
+    return (dw - fp) / (LR * on)
+
+
+def test_single_matrix_beyond_int32_elements(ns, h):
+    rows, cols = 65536, 40000                 # 2.62e9 elements; wide shape 40000 x 65536
+    m, n = cols, rows
+    need = 3 * rows * cols * 4 + 2 * m * n * 2 + 2 * m * m * 2 + (4 << 30)
+    free, _ = torch.cuda.mem_get_info()
+    if free < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free on the device")
+    kr, kc = 256, 384
+    r0, c0 = rows - kr - 40, cols - kc - 8
+    assert r0 * cols + c0 > 2**31 and c0 * rows + r0 > 2**31
+    rng = np.random.default_rng(20240)
+    Wb, Mb, Gb = (rng.standard_normal((kr, kc), dtype=np.float32) for _ in range(3))
+    W = torch.zeros((1, rows, cols), dtype=torch.float32, device="cuda")
+    M = torch.zeros_like(W)
+    G = torch.zeros_like(W)
+    for T, B in ((W, Wb), (M, Mb), (G, Gb)):
+        T[0, r0:r0 + kr, c0:c0 + kc] = torch.from_numpy(B).cuda()
+    ns.muon_step(h, [(rows, cols, 1)], [M], [G], [W], LR, WD, MU, STEPS)
+    ns.muon_last_device_error(h)
+    torch.cuda.synchronize()
+    got = {}
+    for name, T in (("W", W), ("M", M)):
+        got[name] = T[0, r0:r0 + kr, c0:c0 + kc].cpu().numpy()
+        T[0, r0:r0 + kr, c0:c0 + kc] = 0
+        assert int(torch.count_nonzero(T)) == 0, f"{name}: non-zero entries outside the block"
+    del W, M, G
+    torch.cuda.empty_cache()
+    st = o.muon_step_matrix(Wb, Mb, Gb, lr=LR, wd=WD, mu=MU, ns_steps=STEPS)
+    assert ulp_close(got["M"], st.M_new).all()
+    assert update_error(got["W"], st, Wb) <= 2e-2
+
+
+@pytest.mark.parametrize("rows,cols,count", [(8, 1 << 20, 2), (1 << 20, 8, 1), (136, 1 << 20, 1)])
+def test_largest_dimension(ns, h, rows, cols, count):
+    rng = np.random.default_rng(rows + cols)
+    W, M, G = (rng.standard_normal((count, rows, cols), dtype=np.float32) for _ in range(3))
+    dW, dM, dG = (torch.from_numpy(a).cuda() for a in (W, M, G))
+    ns.muon_step(h, [(rows, cols, count)], [dM], [dG], [dW], LR, WD, MU, STEPS)
+    ns.muon_last_device_error(h)
+    Mg, Wg = dM.cpu().numpy(), dW.cpu().numpy()
+    del dW, dM, dG
+    tol = 2e-2 if min(rows, cols) >= 64 else 4e-2
+    for i in range(count):
+        st = o.muon_step_matrix(W[i], M[i], G[i], lr=LR, wd=WD, mu=MU, ns_steps=STEPS)
+        assert ulp_close(Mg[i], st.M_new).all()
+        assert update_error(Wg[i], st, W[i]) <= tol
+
+
+def test_more_matrices_than_one_launch(ns, h):
+    rows, cols, count = 16, 8, 70000          # tall: a batch of 70000 wide 8 x 16 matrices
+    rng = np.random.default_rng(65536)
+    W, M, G = (rng.standard_normal((count, rows, cols), dtype=np.float32) for _ in range(3))
+    dW, dM, dG = (torch.from_numpy(a).cuda() for a in (W, M, G))
+    ns.muon_step(h, [(rows, cols, count)], [dM], [dG], [dW], LR, WD, MU, STEPS)
+    ns.muon_last_device_error(h)
+    Mg, Wg = dM.cpu().numpy(), dW.cpu().numpy()
+    assert ulp_close(Mg, o.momentum_update(M, G, MU)).all()
+    picks = sorted(set([0, 1, 65534, 65535, 65536, count - 1] +
+                       list(rng.choice(count, 40, replace=False))))
+    for i in picks:
+        st = o.muon_step_matrix(W[i], M[i], G[i], lr=LR, wd=WD, mu=MU, ns_steps=STEPS)
+        assert ulp_close(Mg[i], st.M_new).all()
+        assert update_error(Wg[i], st, W[i]) <= 4e-2, f"matrix {i}"
