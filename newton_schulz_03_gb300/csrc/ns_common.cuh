@@ -258,7 +258,11 @@ __device__ __forceinline__ void epilogue_tile_tma(const NsArgs& p, const CUtenso
         if (lane == 0) ptx::bulk_wait_read<1>();
         __syncwarp();
       }
-      uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
+      // The output map uses the 64-byte swizzle: the 16-byte chunk q of row
+      // `lane` sits at chunk q ^ ((lane >> 1) & 3) of the row's 64 bytes, so
+      // the eight rows a quarter-warp writes fall in distinct banks.
+      uint8_t* drow = buf + lane * 64;
+      const int sw = (lane >> 1) & 3;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 u;
@@ -266,7 +270,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const NsArgs& p, const CUtenso
         u.y = pack_bf16(f[q * 8 + 2], f[q * 8 + 3]);
         u.z = pack_bf16(f[q * 8 + 4], f[q * 8 + 5]);
         u.w = pack_bf16(f[q * 8 + 6], f[q * 8 + 7]);
-        dst[q] = u;
+        *reinterpret_cast<uint4*>(drow + ((q ^ sw) << 4)) = u;
       }
       ptx::fence_proxy_async_smem();
       __syncwarp();
