@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -237,6 +238,15 @@ def run_ours(args, world, rank, local):
     sync = torch.cuda.synchronize
     step()
     ns.muon_last_device_error(h, stream)
+    if args.steps is None:
+        # Default K: about 1.5 s per timed pass (enough clock samples), 3..100.
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        sync()
+        t1 = max_over_ranks(a.elapsed_time(b) / 1e3, world, device=torch.device(dev))
+        args.steps = int(max(3, min(100, math.ceil(1.5 / max(t1, 1e-6)))))
     ns.muon_reset_kernel_stats(h)
     graph_ms = None
     if args.graph:
@@ -464,6 +474,8 @@ def run_reference(args, world, rank):
     # Size one step to a bounded sample so the whole run takes minutes.
     n1, t1 = oracle_sample_step(w, 1, 0)
     total_budget = 150.0
+    if args.steps is None:
+        args.steps = 10
     per_step = max(1, int(total_budget / (args.steps + args.warmup) / max(t1, 1e-3)))
     per_step = min(per_step, w.matrices)
     for i in range(args.warmup):
@@ -496,7 +508,8 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about 1.5 s of steps, 3 to 100)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
