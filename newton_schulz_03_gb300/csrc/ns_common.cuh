@@ -162,11 +162,15 @@ __device__ __forceinline__ void epilogue_tile(const NsArgs& p, uint32_t taddr, i
             x[e] = (gcol0 + e < p.out_cols) ? __uint_as_float(static_cast<uint32_t>(a16[e]) << 16)
                                             : 0.f;
         }
-        // B' = b A + c A^2, plus a on the diagonal.
+        // B' = b A + c A^2, plus a on the diagonal (only in the chunk
+        // holding column `grow`).
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float d = (gcol0 + e == grow) ? p.c2 : 0.f;
-          f[e] = fmaf(p.c1, __uint_as_float(v[e]), fmaf(p.c0, x[e], d));
+        for (int e = 0; e < 32; ++e) f[e] = fmaf(p.c1, __uint_as_float(v[e]), p.c0 * x[e]);
+        const int dg = grow - gcol0;
+        if (dg >= 0 && dg < 32) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e == dg) f[e] = fmaf(p.c1, __uint_as_float(v[e]), fmaf(p.c0, x[e], p.c2));
         }
       }
       __nv_bfloat16* orow = out_m + static_cast<int64_t>(grow) * p.out_ld + gcol0;
@@ -246,9 +250,13 @@ __device__ __forceinline__ void epilogue_tile_tma(const NsArgs& p, const CUtenso
                        : 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float d = (gcol0 + e == grow) ? p.c2 : 0.f;
-          f[e] = fmaf(p.c1, __uint_as_float(v[e]), fmaf(p.c0, x[e], d));
+        for (int e = 0; e < 32; ++e) f[e] = fmaf(p.c1, __uint_as_float(v[e]), p.c0 * x[e]);
+        // a on the diagonal: only the chunk holding column `grow` has it.
+        const int dg = grow - gcol0;
+        if (dg >= 0 && dg < 32) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e == dg) f[e] = fmaf(p.c1, __uint_as_float(v[e]), fmaf(p.c0, x[e], p.c2));
         }
       }
       // Reuse a staging buffer only after the store issued from it two
