@@ -108,3 +108,21 @@ def test_plan_rejects_bad_arguments(lib, groups, steps):
 def test_plan_empty_groups(lib):
     info = lib.muon_plan_describe([(64, 64, 0)], ns_steps=5)
     assert info["matrices"] == 0 and info["n_chunks"] == 0 and info["launches_per_step"] == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No fallback: with the shared library absent, the first call raises."""
+    import subprocess
+    import sys
+    code = ("import newton_schulz_03_gb300 as ns\n"
+            "try:\n"
+            "    ns.muon_version()\n"
+            "except ImportError as e:\n"
+            "    print('raised', e)\n"
+            "else:\n"
+            "    print('no error')\n")
+    env = dict(os.environ, MUON_LIB_PATH=str(tmp_path / "absent" / "libmuon_gb300.so"))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.startswith("raised") and "is missing" in r.stdout
