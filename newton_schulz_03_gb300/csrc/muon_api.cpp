@@ -706,6 +706,21 @@ muon_status_t muon_step_host(muon_handle_t h, const muon_group_t* groups, int32_
     pieces.swap(rebuilt);
   }
 
+  // Size the workspace for the largest piece now: growing it inside the
+  // loop would synchronise the device between pieces.
+  {
+    size_t need = 0;
+    for (const Piece& pc : pieces) {
+      const muon_group_t pg{groups[pc.group].rows, groups[pc.group].cols, pc.count, 1.0f};
+      Plan P;
+      st = build_plan(&pg, 1, ns_steps, h->ws_cap, &P);
+      if (st != MUON_OK) return st;
+      need = std::max(need, P.ws_bytes);
+    }
+    st = ensure_workspace(h, need);
+    if (st != MUON_OK) return st;
+  }
+
   const size_t bytes = size_t(kSlots) * 3 * slot_elems * sizeof(float);
   if (h->staging_bytes < bytes) {
     if (h->staging) {
