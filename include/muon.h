@@ -26,7 +26,11 @@
  *  - BF16 values travel as uint16_t bit patterns.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued asynchronously; no entry point synchronises
- *    the stream unless it says so.
+ *    the stream unless it says so.  Kernels are launched with programmatic
+ *    stream serialisation: a kernel may be scheduled while the previous
+ *    kernel in the stream still runs, but reads and writes global memory
+ *    only after that kernel has completed, so stream order is kept.  The
+ *    environment variable MUON_PDL=0 turns this off (plain launches).
  *  - Arguments are validated on the host before anything is enqueued: an
  *    invalid argument returns MUON_ERR_INVALID_ARG and launches nothing.
  *  - A handle is bound to the device that was current when it was created

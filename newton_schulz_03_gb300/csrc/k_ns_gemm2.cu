@@ -15,7 +15,12 @@
 //     barriers (multicast);
 //   * each CTA's TMEM holds its 128 rows x 256 columns of the accumulator
 //     (two accumulators, 512 columns); both CTAs run the epilogue on their
-//     own rows and report back to the even CTA's "tmem empty" barrier.
+//     own rows and report back to the even CTA's "tmem empty" barrier.  The
+//     epilogue writes 32 x 32 BF16 chunks through (64-byte swizzled) shared
+//     memory with TMA stores;
+//   * set-up (barriers, TMEM, tensor-map prefetch) runs before
+//     griddepcontrol.wait, so under programmatic dependent launch it
+//     overlaps the previous kernel's tail.
 // Symmetric products compute AND store only the pair tiles (i, j) with
 // i <= j over 256-blocks (diagonal tiles in full).  Their consumers read a
 // block left of the diagonal, (I, K) with K < I, as the transpose of the
