@@ -164,10 +164,17 @@ def load_peaks():
 
 
 def ns_source_hash() -> str:
+    """Hash of the Newton-Schulz kernel sources with comments and blank
+    lines removed: a profile stays valid across comment-only edits."""
+    import re
     h = hashlib.sha256()
     for p in NS_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode("utf-8"))
     return h.hexdigest()[:16]
 
 
