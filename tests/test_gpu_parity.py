@@ -316,6 +316,28 @@ def test_step_host_pipeline_matches_device_step(ns, h):
         assert err <= NS_TOL + 1e-3
 
 
+def test_step_host_mixed_groups_match_device_step(ns, h):
+    """Host-buffer step over several groups (tall, wide, small) whose first
+    and last pieces are split into ramps of growing and shrinking size
+    equals the device-buffer step bit for bit."""
+    rng = np.random.default_rng(13)
+    groups = [(1024, 512, 40), (512, 1536, 30), (96, 160, 7)]
+    host, devs = [], []
+    for r, c, k in groups:
+        W, M, G = (rng.standard_normal((k, r, c), dtype=np.float32) * np.float32(0.05)
+                   for _ in range(3))
+        host.append([torch.from_numpy(a.copy()).pin_memory() for a in (W, M, G)])
+        devs.append([dev(a) for a in (W, M, G)])
+    ns.muon_step_host(h, groups, [t[1] for t in host], [t[2] for t in host],
+                      [t[0] for t in host], 0.02, 0.1, 0.95, 5)
+    ns.muon_step(h, groups, [t[1] for t in devs], [t[2] for t in devs], [t[0] for t in devs],
+                 0.02, 0.1, 0.95, 5)
+    ns.muon_last_device_error(h)
+    for hw, dw in zip(host, devs):
+        np.testing.assert_array_equal(hw[0].numpy(), dw[0].cpu().numpy())
+        np.testing.assert_array_equal(hw[1].numpy(), dw[1].cpu().numpy())
+
+
 def test_bounded_wait_expires_and_context_survives(ns, h):
     """A device wait that can never complete gives up after its limit,
     reports MUON_ERR_TIMEOUT, and the context keeps working."""
