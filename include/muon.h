@@ -201,7 +201,12 @@ muon_status_t muon_step_ex(muon_handle_t handle, const muon_group_t* groups, int
  * momentum_dev:  count*rows*cols FP32, updated in place.
  * grad_dev:      count*rows*cols FP32.
  * x_wide_dev:    count*m*n BF16 output (m = min, n = max of rows, cols).
- * inv_norm_dev:  count FP32 output. */
+ * inv_norm_dev:  count FP32 output.
+ * A matrix with ||M||_F > 2^60 (about 1.15e18) leaves its x_wide scaled by
+ * an exact power of two 2^e (so that its norm is in [1, 2)) and inv_norm by
+ * 2^-e: x * inv_norm, the Newton-Schulz input, is unchanged, and the
+ * products' FP32 accumulators stay in range.  The same holds inside
+ * muon_step and muon_step_ex. */
 muon_status_t muon_momentum_cast(muon_handle_t handle, int32_t rows, int32_t cols, int32_t count,
                                  float* momentum_dev, const float* grad_dev, float mu,
                                  uint16_t* x_wide_dev, float* inv_norm_dev, void* stream);

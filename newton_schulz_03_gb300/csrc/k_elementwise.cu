@@ -157,23 +157,62 @@ __global__ void __launch_bounds__(kThreads) momentum_cast_kernel(
   if (threadIdx.x == 0) partials[mat * gridDim.x + blockIdx.x] = tot;
 }
 
+// 1/(||U||_F + eps) per matrix, from the cast kernel's partials, summed in
+// FP64 in a fixed order (deterministic).  Range: the cast kernel's FP32
+// partial sums of squares overflow once entries pass ~1.8e19; such a
+// matrix (partials +inf, not NaN) has its norm recomputed here in FP64 from
+// its BF16 copy (within 2^-9 of the FP32 norm).  And the Gram product
+// accumulates X X^T in FP32 before it applies 1/s^2, so a norm above 2^60
+// would overflow its accumulator: such a matrix's BF16 copy is scaled by a
+// power of two 2^e (s * 2^e in [1, 2); exact for every entry that stays
+// normal) and 1/s by 2^-e, so X * inv_norm -- all the products use -- is
+// unchanged.  (Underflowing squares only occur for norms far below eps.)
+constexpr double kNormScaleLimit = 1152921504606846976.0;   // 2^60
+
 __global__ void __launch_bounds__(kThreads) norm_finalize_kernel(
     const float* __restrict__ partials, int per_matrix, float eps, float* __restrict__ inv_norm,
-    int* __restrict__ err) {
+    int* __restrict__ err, uint16_t* __restrict__ X, int64_t x_ld, int64_t x_ms, int m, int n) {
   grid_dep_wait();    // inputs come from the previous kernel of the step
   grid_dep_launch();
   __shared__ double red[kThreads / 32];
+  __shared__ int recompute, scale_exp;
   const int64_t mat = blockIdx.x;
   const float* p = partials + mat * per_matrix;
+  uint16_t* Xm = X != nullptr ? X + mat * x_ms : nullptr;
+  const int64_t total = static_cast<int64_t>(m) * n;
   double acc = 0.0;
   for (int i = threadIdx.x; i < per_matrix; i += kThreads) acc += static_cast<double>(p[i]);
-  const double tot = block_sum(acc, red);
+  double tot = block_sum(acc, red);   // valid in thread 0
+  if (threadIdx.x == 0) recompute = (isinf(tot) && Xm != nullptr) ? 1 : 0;
+  __syncthreads();
+  if (recompute) {
+    double a2 = 0.0;
+    for (int64_t i = threadIdx.x; i < total; i += kThreads) {
+      const double v = bf16_to_f32(Xm[(i / n) * x_ld + i % n]);
+      a2 = fma(v, v, a2);
+    }
+    tot = block_sum(a2, red);
+  }
   if (threadIdx.x == 0) {
+    int e = 0;
     if (!isfinite(tot)) {
       atomicOr(err, kDevErrNonFinite);
       inv_norm[mat] = 0.f;
     } else {
-      inv_norm[mat] = static_cast<float>(1.0 / (sqrt(tot) + static_cast<double>(eps)));
+      const double s = sqrt(tot);
+      if (s > kNormScaleLimit && Xm != nullptr) e = -ilogb(s);
+      inv_norm[mat] = static_cast<float>(1.0 / ((s + static_cast<double>(eps)) * ldexp(1.0, e)));
+    }
+    scale_exp = e;
+  }
+  __syncthreads();
+  const int e = scale_exp;
+  if (e != 0) {
+    // Two normal factors (2^e alone may be below the FP32 normal range).
+    const float f1 = ldexpf(1.0f, e / 2), f2 = ldexpf(1.0f, e - e / 2);
+    for (int64_t i = threadIdx.x; i < total; i += kThreads) {
+      uint16_t* q = Xm + (i / n) * x_ld + i % n;
+      *q = bf16_bits(bf16_to_f32(*q) * f1 * f2);
     }
   }
 }
@@ -310,10 +349,11 @@ cudaError_t launch_momentum_cast(int rows, int cols, int count, float* M, const 
 }
 
 cudaError_t launch_norm_finalize(const float* partials, int per_matrix, int count, float eps,
-                                 float* inv_norm, int* err, cudaStream_t stream) {
+                                 float* inv_norm, int* err, uint16_t* x, int64_t x_ld,
+                                 int64_t x_ms, int m, int n, cudaStream_t stream) {
   if (count <= 0) return cudaSuccess;
   return launch_pdl(norm_finalize_kernel, dim3(count), dim3(kThreads), 0, stream, partials,
-                    per_matrix, eps, inv_norm, err);
+                    per_matrix, eps, inv_norm, err, x, x_ld, x_ms, m, n);
 }
 
 cudaError_t launch_apply_update(int rows, int cols, int count, float* W, const uint16_t* O,

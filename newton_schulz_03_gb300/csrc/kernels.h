@@ -27,8 +27,11 @@ cudaError_t launch_momentum_cast(int rows, int cols, int count, float* M, const 
                                  float* partials, cudaStream_t stream, bool nesterov = false);
 
 // inv_norm[mat] <- 1 / (sqrt(sum of partials of mat) + eps); flags NaN/Inf.
+// A matrix whose norm exceeds 2^60 has its BF16 copy x (m x n, pitches in
+// elements) scaled by 2^e and inv_norm by 2^-e (see the kernel).
 cudaError_t launch_norm_finalize(const float* partials, int per_matrix, int count, float eps,
-                                 float* inv_norm, int* err, cudaStream_t stream);
+                                 float* inv_norm, int* err, uint16_t* x, int64_t x_ld,
+                                 int64_t x_ms, int m, int n, cudaStream_t stream);
 
 // Step 5: W <- W (1 - lr wd) - lr scale O, O in wide layout (pitches in
 // elements), transposed back when rows > cols.

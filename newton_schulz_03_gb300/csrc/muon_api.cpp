@@ -552,7 +552,7 @@ muon_status_t step_impl(muon_handle_t h, const muon_group_t* groups, int32_t n_g
     {
       LaunchScope Ls(h, MUON_KERNEL_NORM, s);
       cudaError_t e = muon::launch_norm_finalize(part, L.tiles, c.count, MUON_NORM_EPS, inv,
-                                                 h->dev_err, s);
+                                                 h->dev_err, x0, L.ldx, xms, c.m, c.n, s);
       if (e != cudaSuccess) return cuda_fail(e, "norm launch");
     }
     // The iterates alternate between x0 and x1, starting from x0; the
@@ -829,7 +829,7 @@ muon_status_t muon_momentum_cast(muon_handle_t h, int32_t rows, int32_t cols, in
   }
   LaunchScope Ls(h, MUON_KERNEL_NORM, s);
   cudaError_t e = muon::launch_norm_finalize(part, tiles, count, MUON_NORM_EPS, inv_norm,
-                                             h->dev_err, s);
+                                             h->dev_err, x_wide, n, int64_t(m) * n, m, n, s);
   if (e != cudaSuccess) return cuda_fail(e, "norm launch");
   return MUON_OK;
 }

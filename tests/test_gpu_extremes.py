@@ -111,3 +111,44 @@ def test_more_matrices_than_one_launch(ns, h):
         st = o.muon_step_matrix(W[i], M[i], G[i], lr=LR, wd=WD, mu=MU, ns_steps=STEPS)
         assert ulp_close(Mg[i], st.M_new).all()
         assert update_error(Wg[i], st, W[i]) <= 4e-2, f"matrix {i}"
+
+
+@pytest.mark.parametrize("scale", [1e25, 1e15, 1e-25])
+def test_extreme_momentum_scales(ns, h, scale):
+    """The method is scale-invariant up to its 1e-7 in the norm.  At 1e25
+    the FP32 partial sums of squares overflow (the norm is recomputed in
+    FP64) and the norm (~6e27) is above 2^60, where the Gram product's FP32
+    accumulator would overflow: the BF16 copy must come back scaled by a
+    power of two with X * inv_norm unchanged, and the orthogonalised update
+    must still match the oracle.  1e15 stays below both limits; at 1e-25
+    the 1e-7 dominates the norm and the iteration is linear."""
+    rows, cols, count = 384, 256, 2            # tall: runs as 256 x 384
+    m, n = min(rows, cols), max(rows, cols)
+    rng = np.random.default_rng(int(np.log10(scale)) + 100)
+    M = (rng.standard_normal((count, rows, cols)) * scale).astype(np.float32)
+    G = (rng.standard_normal((count, rows, cols)) * scale).astype(np.float32)
+    dM, dG = torch.from_numpy(M.copy()).cuda(), torch.from_numpy(G).cuda()
+    X = torch.zeros((count, m, n), dtype=torch.int16, device="cuda")
+    inv = torch.zeros(count, dtype=torch.float32, device="cuda")
+    ns.muon_momentum_cast(h, rows, cols, count, dM, dG, MU, X, inv)
+    O = torch.zeros_like(X)
+    ns.muon_newton_schulz_bf16(h, m, n, count, X, O, inv, STEPS)
+    ns.muon_last_device_error(h)
+    Xg = o.bf16_bits_to_f64(X.cpu().numpy().view(np.uint16))
+    Og = o.bf16_bits_to_f64(O.cpu().numpy().view(np.uint16))
+    invg = inv.cpu().numpy().astype(np.float64)
+    Mg = dM.cpu().numpy()
+    for i in range(count):
+        assert ulp_close(Mg[i], o.momentum_update(M[i], G[i], MU)).all()
+        Mn = Mg[i]                               # the momentum the GPU cast
+        Xw, _ = o.to_wide(o.bf16_rne(Mn))
+        s = o.frobenius_scale(Mn)
+        # the normalised input the products see (above ~1.8e19 per entry the
+        # norm comes from the BF16 copy, within 2^-9 of the FP32 norm)
+        rtol = 2e-6 if scale < 1e18 else 1e-3
+        np.testing.assert_allclose(Xg[i] * invg[i], Xw / s, rtol=rtol, atol=0.0)
+        ref = o.newton_schulz(Xw, s, STEPS)
+        err = np.linalg.norm(Og[i] - ref) / np.linalg.norm(ref)
+        assert err <= 2e-2, f"scale {scale:g} matrix {i}: {err:.3e}"
+    if scale > 2.0**60:
+        assert np.max(np.abs(Xg)) < 4.0      # the working copy was brought to unit scale
