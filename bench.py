@@ -343,6 +343,8 @@ def run_ours(args, world, rank, local):
         "tflops_algorithmic": round(tflops, 1),
         "pct_of_bf16_peak": round(100 * tflops / peak, 2),
         "tflops_dense_equivalent": round(tflops * dense_over_alg(w), 1),
+        "tflops_performed": round(world * plan["ns_performed_flops"] * layers * args.steps
+                                  / secs / 1e12, 1),
         "gpu_launches": gpu_launches,
         "graph_replay_ms_per_step": round(graph_ms, 4) if graph_ms is not None else None,
         "ms_per_step_with_kernel_events": round(secs_ev * 1e3 / args.steps, 4),

@@ -22,7 +22,7 @@ STATUS_NAMES = {
     7: "MUON_ERR_NO_DEVICE",
 }
 KERNEL_NAMES = ("momentum_cast", "norm", "ns_gram", "ns_poly", "ns_update", "apply", "scale",
-                "adamw")
+                "adamw", "ns_gram_recur")
 N_KERNELS = len(KERNEL_NAMES)
 
 # Symbols the header declares (checked by the CPU test-suite).
@@ -71,7 +71,7 @@ class _PlanInfo(ctypes.Structure):
     _fields_ = [("n_batches", ctypes.c_int32), ("n_chunks", ctypes.c_int32),
                 ("max_chunk_matrices", ctypes.c_int32), ("matrices", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t), ("ns_algorithmic_flops", ctypes.c_double),
-                ("launches_per_step", ctypes.c_int64)]
+                ("launches_per_step", ctypes.c_int64), ("ns_performed_flops", ctypes.c_double)]
 
 
 _lib = None

@@ -18,6 +18,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -61,13 +62,29 @@ int64_t max_count_per_launch(int m, int n) {
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Gram recurrence.  B' = a I + b A + c A^2 is a polynomial in A = X X^T, so
+// it commutes with A and the next Gram matrix is
+//   X' X'^T = B' X X^T B' = (B' A) B',
+// two symmetric m x m x m products (2 m^3 flops, K = m) instead of one
+// m x m x n product (m^2 n): fewer flops when n > 2 m.  It is used for
+// iterations 1.. of wide batches (n >= 2.5 m) on the CTA-pair path; the
+// first Gram matrix is always X X^T.  MUON_NS_RECUR=0 turns it off.
+bool use_gram_recurrence(int m, int n) {
+  static const bool on = [] {
+    const char* v = std::getenv("MUON_NS_RECUR");
+    return !(v != nullptr && std::strcmp(v, "0") == 0);
+  }();
+  return on && muon::ns_symmul_supported(m) && 2 * int64_t(n) >= 5 * int64_t(m);
+}
 int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
 
 // Workspace layout of one chunk of `cap` matrices of wide shape m x n.
 struct ChunkLayout {
   int64_t ldx, ldm;  // row pitches (elements) of X and of A/B
   int tiles;         // elementwise tiles per matrix (norm partials)
-  size_t off_x0, off_x1, off_a, off_b, off_part, off_inv, bytes;
+  bool recur;        // Gram recurrence in use: C holds B' A
+  size_t off_x0, off_x1, off_a, off_b, off_c, off_part, off_inv, bytes;
 };
 
 ChunkLayout chunk_layout(int m, int n, int64_t cap) {
@@ -82,6 +99,8 @@ ChunkLayout chunk_layout(int m, int n, int64_t cap) {
   L.off_x1 = off; off += xb;
   L.off_a = off; off += ab;
   L.off_b = off; off += ab;
+  L.recur = use_gram_recurrence(m, n);
+  L.off_c = off; off += L.recur ? ab : 0;
   L.off_part = off; off += align_up(size_t(cap) * L.tiles * 4, kAlign);
   L.off_inv = off; off += align_up(size_t(cap) * 4, kAlign);
   L.bytes = off;
@@ -90,7 +109,8 @@ ChunkLayout chunk_layout(int m, int n, int64_t cap) {
 
 size_t per_matrix_bytes(int m, int n) {
   const int64_t ldx = pad8(n), ldm = pad8(m);
-  return size_t(2) * m * ldx * 2 + size_t(2) * m * ldm * 2 +
+  const int sq = use_gram_recurrence(m, n) ? 3 : 2;   // A, B' (and C)
+  return size_t(2) * m * ldx * 2 + size_t(sq) * m * ldm * 2 +
          size_t(muon::ew_tiles_per_matrix(m, n)) * 4 + 4;
 }
 
@@ -114,6 +134,7 @@ struct Plan {
   int64_t matrices = 0;
   size_t ws_bytes = 0;
   double flops = 0.0;
+  double flops_performed = 0.0;
   int64_t launches = 0;
 };
 
@@ -172,6 +193,12 @@ muon_status_t build_plan(const muon_group_t* groups, int32_t n_groups, int32_t n
     P.ws_bytes = std::max(P.ws_bytes, chunk_layout(m, n, cap).bytes);
     P.matrices += total;
     P.flops += double(total) * ns_steps * (3.0 * m * double(m) * n + double(m) * m * m);
+    {
+      const double gram = double(m) * m * n, sq = double(m) * m * m, upd = 2.0 * gram;
+      const double later = (use_gram_recurrence(m, n) ? 2.0 * sq : gram) + sq + upd;
+      P.flops_performed +=
+          ns_steps > 0 ? double(total) * ((gram + sq + upd) + (ns_steps - 1) * later) : 0.0;
+    }
     // Cut the batch into chunks of at most `cap` matrices.
     Chunk cur{m, n, 0, {}};
     for (int g : b.second) {
@@ -192,6 +219,7 @@ muon_status_t build_plan(const muon_group_t* groups, int32_t n_groups, int32_t n
   for (const Chunk& c : P.chunks) {
     P.max_chunk = std::max(P.max_chunk, c.count);
     P.launches += 2 * static_cast<int64_t>(c.segs.size()) + 1 + (ns_steps > 0 ? 3 * ns_steps : 1);
+    if (ns_steps > 1 && use_gram_recurrence(c.m, c.n)) P.launches += ns_steps - 1;
   }
   *plan = std::move(P);
   return MUON_OK;
@@ -292,10 +320,12 @@ struct Coeffs {
 // ns_steps iterations on `count` wide matrices.  Reads x (never written);
 // iteration k writes dst[k]; the last one lands in `out`.  A, B: scratch.
 // `sched` holds the (a, b, c) of every iteration (at least `steps` entries).
+// C: scratch m x m for the Gram recurrence (ptr NULL: every Gram matrix is
+// computed as X X^T).
 muon_status_t run_newton_schulz(muon_handle_t h, int m, int n, int count, muon::BatchView x,
                                 muon::BatchView out, muon::BatchView other, muon::BatchView A,
-                                muon::BatchView B, const float* inv_norm, int steps,
-                                const Coeffs* sched, cudaStream_t s) {
+                                muon::BatchView B, muon::BatchView C, const float* inv_norm,
+                                int steps, const Coeffs* sched, cudaStream_t s) {
   if (steps == 0) {
     LaunchScope L(h, MUON_KERNEL_SCALE, s);
     cudaError_t e = muon::launch_scale_bf16(
@@ -312,12 +342,27 @@ muon_status_t run_newton_schulz(muon_handle_t h, int m, int n, int count, muon::
     const float* inv = (k == 0) ? inv_norm : nullptr;
     const Coeffs co = sched[k];
     cudaError_t e;
-    {
-      LaunchScope L(h, MUON_KERNEL_NS_GRAM, s);
-      e = muon::ns_launch_gram(m, n, count, src, A, inv, h->dev_err, h->num_sms, s);
+    if (k > 0 && C.ptr != nullptr) {
+      // A_k = B'_{k-1} A_{k-1} B'_{k-1}: C = B' A, then A = C B'.
+      {
+        LaunchScope L(h, MUON_KERNEL_NS_GRAM_RECUR, s);
+        e = muon::ns_launch_symmul(m, count, B, A, C, h->dev_err, h->num_sms, s);
+      }
+      if (e == cudaSuccess) {
+        LaunchScope L(h, MUON_KERNEL_NS_GRAM_RECUR, s);
+        e = muon::ns_launch_symmul(m, count, C, B, A, h->dev_err, h->num_sms, s);
+      }
+      if (e != cudaSuccess)
+        return fail(MUON_ERR_CUDA, "gram recurrence launch: %s %s", cudaGetErrorString(e),
+                    muon::ns_last_encode_error());
+    } else {
+      {
+        LaunchScope L(h, MUON_KERNEL_NS_GRAM, s);
+        e = muon::ns_launch_gram(m, n, count, src, A, inv, h->dev_err, h->num_sms, s);
+      }
+      if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "gram launch: %s %s",
+                                        cudaGetErrorString(e), muon::ns_last_encode_error());
     }
-    if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "gram launch: %s %s", cudaGetErrorString(e),
-                                      muon::ns_last_encode_error());
     {
       LaunchScope L(h, MUON_KERNEL_NS_POLY, s);
       e = muon::ns_launch_poly(m, count, A, B, co.a, co.b, co.c, h->dev_err, h->num_sms, s);
@@ -471,6 +516,7 @@ muon_status_t muon_plan_describe(const muon_group_t* groups, int32_t n_groups, i
   out->workspace_bytes = P.ws_bytes;
   out->ns_algorithmic_flops = P.flops;
   out->launches_per_step = P.launches;
+  out->ns_performed_flops = P.flops_performed;
   return MUON_OK;
 }
 
@@ -561,7 +607,8 @@ muon_status_t step_impl(muon_handle_t h, const muon_group_t* groups, int32_t n_g
     uint16_t* oth = (fin == x0) ? x1 : x0;
     const muon::BatchView vx0{x0, L.ldx, xms}, vfin{fin, L.ldx, xms}, voth{oth, L.ldx, xms};
     const muon::BatchView vA{A, L.ldm, ams}, vB{B, L.ldm, ams};
-    st = run_newton_schulz(h, c.m, c.n, c.count, vx0, vfin, voth, vA, vB, inv, ns_steps,
+    const muon::BatchView vC{L.recur ? ws + L.off_c : nullptr, L.ldm, ams};
+    st = run_newton_schulz(h, c.m, c.n, c.count, vx0, vfin, voth, vA, vB, vC, inv, ns_steps,
                            o.sched.data(), s);
     if (st != MUON_OK) return st;
     for (const Segment& sg : c.segs) {
@@ -859,13 +906,17 @@ muon_status_t muon_newton_schulz_bf16(muon_handle_t h, int32_t m, int32_t n, int
   const size_t xbytes = size_t(count) * m * n * 2;
   const uintptr_t xb = reinterpret_cast<uintptr_t>(x), ob = reinterpret_cast<uintptr_t>(out);
   if (xb < ob + xbytes && ob < xb + xbytes) return fail(MUON_ERR_INVALID_ARG, "x and out overlap");
-  // Scratch: one more X buffer and A, B -- in chunks that fit the cap.
-  const size_t pm = align_up(size_t(m) * n * 2, 16) + 2 * align_up(size_t(m) * m * 2, 16);
+  // Scratch: one more X buffer and A, B (and C for the Gram recurrence) --
+  // in chunks that fit the cap.
+  const bool recur = use_gram_recurrence(m, n);
+  const int nsq = recur ? 3 : 2;
+  const size_t pm = align_up(size_t(m) * n * 2, 16) + nsq * align_up(size_t(m) * m * 2, 16);
   int64_t cap = static_cast<int64_t>(h->ws_cap / pm);
   if (cap < 1) cap = 1;
   if (cap > count) cap = count;
   cap = std::min(cap, max_count_per_launch(m, n));
-  const size_t need = align_up(size_t(cap) * m * n * 2, kAlign) + 2 * align_up(size_t(cap) * m * m * 2, kAlign);
+  const size_t need = align_up(size_t(cap) * m * n * 2, kAlign) +
+                     nsq * align_up(size_t(cap) * m * m * 2, kAlign);
   st = ensure_workspace(h, need);
   if (st != MUON_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(h->ws);
@@ -873,13 +924,16 @@ muon_status_t muon_newton_schulz_bf16(muon_handle_t h, int32_t m, int32_t n, int
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + align_up(size_t(cap) * m * n * 2, kAlign));
   uint16_t* B = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(A) +
                                             align_up(size_t(cap) * m * m * 2, kAlign));
+  uint16_t* Cm = recur ? reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(B) +
+                                                     align_up(size_t(cap) * m * m * 2, kAlign))
+                       : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t xms = int64_t(m) * n, ams = int64_t(m) * m;
   for (int64_t done = 0; done < count; done += cap) {
     const int take = static_cast<int>(std::min<int64_t>(count - done, cap));
     const muon::BatchView vx{x + done * xms, n, xms}, vo{out + done * xms, n, xms};
-    const muon::BatchView vt{other, n, xms}, vA{A, m, ams}, vB{B, m, ams};
-    st = run_newton_schulz(h, m, n, take, vx, vo, vt, vA, vB, inv_norm + done, ns_steps,
+    const muon::BatchView vt{other, n, xms}, vA{A, m, ams}, vB{B, m, ams}, vC{Cm, m, ams};
+    st = run_newton_schulz(h, m, n, take, vx, vo, vt, vA, vB, vC, inv_norm + done, ns_steps,
                            sched.data(), s);
     if (st != MUON_OK) return st;
   }

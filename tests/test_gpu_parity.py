@@ -237,6 +237,28 @@ def test_step_chunked_workspace(ns, ):
         run_step_and_check(ns, hh.value, [(r, c, k)], arrays)
 
 
+@pytest.mark.parametrize("m,n,count", [(256, 1024, 3), (392, 1000, 2), (512, 1280, 2)])
+def test_gram_recurrence_path(ns, h, m, n, count):
+    """Wide batches (n >= 2.5 m) on the CTA-pair path form the Gram matrix
+    of iterations 1.. as B' A B' (two symmetric m x m products) instead of
+    X X^T: the launches show it, and the result matches the oracle."""
+    rng = np.random.default_rng(m + n)
+    Xb = o.bf16_rne_bits(rng.standard_normal((count, m, n), dtype=np.float32))
+    Xf = o.bf16_bits_to_f64(Xb)
+    inv = np.array([1.0 / (np.linalg.norm(Xf[i]) + o.NORM_EPS) for i in range(count)],
+                   dtype=np.float32)
+    out = torch.zeros((count, m, n), dtype=torch.int16, device="cuda")
+    ns.muon_reset_kernel_stats(h)
+    ns.muon_newton_schulz_bf16(h, m, n, count, dev(Xb.view(np.int16)), out, dev(inv), 5)
+    ns.muon_last_device_error(h)
+    st = ns.muon_kernel_stats(h)
+    assert st["launches"]["ns_gram"] == 1 and st["launches"]["ns_gram_recur"] == 8
+    got = o.bf16_bits_to_f64(u16(out))
+    for i in range(count):
+        ref = o.newton_schulz(Xf[i], 1.0 / float(inv[i]), 5)
+        assert rel_fro(got[i], ref) <= NS_TOL
+
+
 def test_step_host_buffers(ns, h):
     rng = np.random.default_rng(11)
     r, c, k = 192, 96, 3
