@@ -81,7 +81,7 @@ typedef enum {
   MUON_KERNEL_APPLY = 5,          /* W = W (1 - lr wd) - lr s O */
   MUON_KERNEL_SCALE = 6,          /* ns_steps == 0: O = X / s */
   MUON_KERNEL_ADAMW = 7,          /* AdamW companion */
-  MUON_KERNEL_NS_GRAM_RECUR = 8,  /* next Gram matrix as B' A B' (two m x m products) */
+  MUON_KERNEL_NS_SYMMUL = 8,      /* product form: m x m products B'A, (B'A)B', B'Q */
   MUON_KERNEL_COUNT = 9
 } muon_kernel_t;
 
@@ -101,10 +101,14 @@ typedef struct {
   double ns_algorithmic_flops;/* sum over matrices of ns_steps*(3 m^2 n + m^3) */
   int64_t launches_per_step;  /* kernel launches one muon_step makes */
   double ns_performed_flops;  /* the same count for the products the kernels
-                                 run: with the Gram recurrence (wide batches,
-                                 n >= 2.5 m, m > 128) iterations after the
-                                 first form the Gram matrix in 2 m^3 instead
-                                 of m^2 n */
+                                 run: wide batches (n >= 2.5 m, m > 128,
+                                 ns_steps >= 2) use the product form,
+                                 3 m^2 n + (4 ns_steps - 3) m^3 per matrix */
+  double ns_kind_flops[4];    /* ns_performed_flops by kernel class: Gram,
+                                 square, update, symmetric m x m product
+                                 (symmetric products counted at half) */
+  int64_t ns_kind_matrix_launches[4]; /* per class: sum over launches of the
+                                 matrices each launch covers */
 } muon_plan_info_t;
 
 /* Default Newton-Schulz configuration: quintic coefficients (a, b, c),

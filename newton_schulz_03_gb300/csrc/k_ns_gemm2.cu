@@ -167,8 +167,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           } else {
             ptx::tma_load_3d_pair(sa, &tmap_a, full_leader, kb * kBK, rowA, mat);
           }
-          if (MODE == kUpdate || (kSymB && kblk < tj)) {
-            // X as the MN-major operand, or the transpose of a stored block.
+          if (MODE == kUpdate || (kSymB && kblk <= tj)) {
+            // X as the MN-major operand, or a stored block of a symmetric
+            // right-hand operand R read as R[k, j] (MN-major).  The diagonal
+            // block is read this way too, so the product is L R with both
+            // diagonal blocks as stored (their rounding leaves them not quite
+            // symmetric; L R^T there would differ, and the product form of the
+            // iteration amplifies that difference).
             const CUtensorMap* mb = (MODE == kUpdate) ? &tmap_b : &tmap_bt;
             if (p.mn4d) {
               ptx::tma_load_4d_pair(sb, mb, full_leader, 0, kb * kBK, colB / 64, mat);
@@ -225,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < num_kb; ++kb) {
           const int kblk = (kb * kBK) / kPairM;
           const uint32_t a_mn = (kSymA && kblk < ti) ? 1u : 0u;
-          const uint32_t b_mn = (MODE == kUpdate || (kSymB && kblk < tj)) ? 1u : 0u;
+          const uint32_t b_mn = (MODE == kUpdate || (kSymB && kblk <= tj)) ? 1u : 0u;
           const uint32_t idesc = ptx::idesc_bf16_f32(kPairM, kPairN, a_mn, b_mn);
           if (!ptx::mbar_wait_cluster(&full[stage], phase, abort_flag)) {
             ok = false;
