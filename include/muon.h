@@ -225,7 +225,12 @@ muon_status_t muon_momentum_cast(muon_handle_t handle, int32_t rows, int32_t col
  * matrices m x n (m <= n), each pre-scaled by inv_norm[i]:
  *   X0 = inv_norm[i] * x[i]; ns_steps times X = a X + (b A + c A^2) X,
  *   A = X X^T.  Gram and square products compute only upper-triangle
- *   tiles and mirror them.
+ *   tiles.  Wide batches (n >= 2.5 m, m > 128, ns_steps >= 2) evaluate the
+ *   same iteration in product form: B'_k = a I + b A_k + c A_k^2 commute,
+ *   so A_{k+1} = B'_k A_k B'_k and X_N = (B'_{N-1} ... B'_0) X0, with
+ *   symmetric m x m products only and one final product with X0 (equal in
+ *   exact arithmetic; within the same error bar; MUON_NS_PRODUCT=0 in the
+ *   environment turns it off).
  * x_dev, out_dev: count*m*n BF16, 16-byte aligned, must not overlap.
  * inv_norm_dev:   count FP32 (device).
  * coeffs_host:    3 floats (a, b, c) or NULL for the defaults.
