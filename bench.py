@@ -37,13 +37,7 @@ METRIC = "NS-orthogonalised matrices/s and TFLOPS (% of GB300 BF16 peak); muon_s
 UNIT = "matrices/s"
 DEFAULT_WORKLOAD = "l24_attention"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-NS_KINDS = ("ns_gram", "ns_poly", "ns_update", "ns_symmul")
-NS_KERNEL_NAMES = {
-    "ns_gram": "<gram> (A = alpha X X^T)",
-    "ns_poly": "<poly> (B' = aI + bA + cA^2)",
-    "ns_update": "<update> (X' = alpha B' X)",
-    "ns_symmul": "<symmul> (C = L R, symmetric m x m)",
-}
+DOMINANT = "ns_update"
 NS_SOURCES = ("newton_schulz_03_gb300/csrc/k_ns_gemm.cu", "newton_schulz_03_gb300/csrc/k_ns_gemm2.cu",
               "newton_schulz_03_gb300/csrc/ns_common.cuh", "newton_schulz_03_gb300/csrc/sm103_ptx.cuh")
 
@@ -184,12 +178,12 @@ def ns_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kind: str, workload: str, matrices_per_launch: float):
+def profiled_traffic(workload: str, matrices_per_launch: float):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source.  The summary gives
     bytes per matrix (traffic grows with the matrix count); one launch covers
     ``matrices_per_launch`` matrices on average."""
-    path = os.path.join(ROOT, "profiles", f"{kind}_{workload.split('[')[0]}.txt")
+    path = os.path.join(ROOT, "profiles", f"{DOMINANT}_{workload.split('[')[0]}.txt")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -299,44 +293,37 @@ def run_ours(args, world, rank, local):
     ms_per_step = secs * 1e3 / args.steps
     flops_step = plan["ns_algorithmic_flops"] * layers
     tflops = world * flops_step * args.steps / secs / 1e12
-    tflops_perf = world * plan["ns_performed_flops"] * layers * args.steps / secs / 1e12
 
     peaks, peak_src = load_peaks()
     peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    # Dominant kernel: the Newton-Schulz kernel class with the most device
-    # time (the update product on square shapes, the symmetric m x m product
-    # in the product form of wide batches); its flops per step come from the
-    # plan (symmetric products counted at half).
+    # Dominant kernel: the update product X' = aX + BX, 2 m^2 n flops per matrix.
+    upd_flops_step = sum(c * 2.0 * mm * mm * nn for (mm, nn), c in w.wide_batches().items()) \
+        * w.ns_steps * layers
+    upd_launches = stats["launches"][DOMINANT]
+    upd_ms = stats["total_ms"][DOMINANT]
     steps_recorded = args.steps + args.warmup
-    dom = max(NS_KINDS, key=lambda k: stats["total_ms"][k])
-    dom_launches = stats["launches"][dom]
-    dom_ms = stats["total_ms"][dom]
-    dom_flops_step = plan["ns_kind_flops"][dom] * layers
-    achieved = (dom_flops_step * steps_recorded) / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else None
-    ns_ms = sum(stats["total_ms"][k] for k in NS_KINDS)
+    achieved = (upd_flops_step * steps_recorded) / (upd_ms / 1e3) / 1e12 if upd_ms > 0 else None
+    ns_ms = sum(stats["total_ms"][k] for k in ("ns_gram", "ns_poly", "ns_update"))
     ns_tflops = (flops_step * steps_recorded) / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
-    ns_tflops_perf = (plan["ns_performed_flops"] * layers * steps_recorded) / (ns_ms / 1e3) / 1e12 \
-        if ns_ms > 0 else None
     kernel_share = {k: round(v / max(sum(stats["total_ms"].values()), 1e-9), 4)
                     for k, v in stats["total_ms"].items() if v > 0}
-    dom_matrix_launches = plan["ns_kind_matrix_launches"][dom] * layers
-    traffic = profiled_traffic(dom, w.name, dom_matrix_launches * steps_recorded / dom_launches) \
-        if dom_launches else None
+    upd_matrices_step = sum(w.wide_batches().values()) * w.ns_steps * layers
+    traffic = profiled_traffic(w.name, upd_matrices_step * steps_recorded / upd_launches) \
+        if upd_launches else None
     roofline = {
-        "kernel": ("ns_gemm_pair_kernel" if min(m for m, _ in w.wide_batches()) > 128
-                   else "ns_gemm_kernel") + NS_KERNEL_NAMES[dom],
+        "kernel": ("ns_gemm_pair_kernel<update>" if min(m for m, _ in w.wide_batches()) > 128
+                   else "ns_gemm_kernel<update,256>") + " (X' = alpha B' X)",
         "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
         "peak": peak, "unit": "TFLOP/s",
         "frac": round(achieved / peak, 4) if achieved else None,
         "peak_source": f"{peak_src} bf16_tflops_sustained (of {peak_src})",
         "frac_of_burst": round(achieved / burst, 4) if achieved else None,
         "traffic": traffic,
-        "launches": dom_launches,
-        "avg_launch_ms": round(dom_ms / dom_launches, 4) if dom_launches else None,
+        "launches": upd_launches,
+        "avg_launch_ms": round(upd_ms / upd_launches, 4) if upd_launches else None,
         "ns_engine_tflops": round(ns_tflops, 1) if ns_tflops else None,
         "ns_engine_frac": round(ns_tflops / peak, 4) if ns_tflops else None,
-        "ns_engine_tflops_performed": round(ns_tflops_perf, 1) if ns_tflops_perf else None,
         "kernel_time_share": kernel_share,
     }
     line = {
@@ -353,13 +340,9 @@ def run_ours(args, world, rank, local):
                   % (sum(g.numel for g in w.groups) * 12 / 1e9),
             "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
         },
-        # The method's count, 5 (3 m^2 n + m^3) per matrix (symmetric products
-        # at half): an effective rate once wide batches run the product form.
         "tflops_algorithmic": round(tflops, 1),
+        "pct_of_bf16_peak": round(100 * tflops / peak, 2),
         "tflops_dense_equivalent": round(tflops * dense_over_alg(w), 1),
-        # What the kernels execute (same counting), and its share of the peak.
-        "tflops_performed": round(tflops_perf, 1),
-        "pct_of_bf16_peak": round(100 * tflops_perf / peak, 2),
         "gpu_launches": gpu_launches,
         "graph_replay_ms_per_step": round(graph_ms, 4) if graph_ms is not None else None,
         "ms_per_step_with_kernel_events": round(secs_ev * 1e3 / args.steps, 4),

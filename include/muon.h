@@ -81,8 +81,7 @@ typedef enum {
   MUON_KERNEL_APPLY = 5,          /* W = W (1 - lr wd) - lr s O */
   MUON_KERNEL_SCALE = 6,          /* ns_steps == 0: O = X / s */
   MUON_KERNEL_ADAMW = 7,          /* AdamW companion */
-  MUON_KERNEL_NS_SYMMUL = 8,      /* product form: m x m products B'A, (B'A)B', B'Q */
-  MUON_KERNEL_COUNT = 9
+  MUON_KERNEL_COUNT = 8
 } muon_kernel_t;
 
 typedef struct {
@@ -100,15 +99,6 @@ typedef struct {
   size_t workspace_bytes;     /* device workspace the plan needs */
   double ns_algorithmic_flops;/* sum over matrices of ns_steps*(3 m^2 n + m^3) */
   int64_t launches_per_step;  /* kernel launches one muon_step makes */
-  double ns_performed_flops;  /* the same count for the products the kernels
-                                 run: wide batches (n >= 2.5 m, m > 128,
-                                 ns_steps >= 2) use the product form,
-                                 3 m^2 n + (4 ns_steps - 3) m^3 per matrix */
-  double ns_kind_flops[4];    /* ns_performed_flops by kernel class: Gram,
-                                 square, update, symmetric m x m product
-                                 (symmetric products counted at half) */
-  int64_t ns_kind_matrix_launches[4]; /* per class: sum over launches of the
-                                 matrices each launch covers */
 } muon_plan_info_t;
 
 /* Default Newton-Schulz configuration: quintic coefficients (a, b, c),
@@ -225,12 +215,7 @@ muon_status_t muon_momentum_cast(muon_handle_t handle, int32_t rows, int32_t col
  * matrices m x n (m <= n), each pre-scaled by inv_norm[i]:
  *   X0 = inv_norm[i] * x[i]; ns_steps times X = a X + (b A + c A^2) X,
  *   A = X X^T.  Gram and square products compute only upper-triangle
- *   tiles.  Wide batches (n >= 2.5 m, m > 128, ns_steps >= 2) evaluate the
- *   same iteration in product form: B'_k = a I + b A_k + c A_k^2 commute,
- *   so A_{k+1} = B'_k A_k B'_k and X_N = (B'_{N-1} ... B'_0) X0, with
- *   symmetric m x m products only and one final product with X0 (equal in
- *   exact arithmetic; within the same error bar; MUON_NS_PRODUCT=0 in the
- *   environment turns it off).
+ *   tiles and mirror them.
  * x_dev, out_dev: count*m*n BF16, 16-byte aligned, must not overlap.
  * inv_norm_dev:   count FP32 (device).
  * coeffs_host:    3 floats (a, b, c) or NULL for the defaults.

@@ -22,7 +22,7 @@ STATUS_NAMES = {
     7: "MUON_ERR_NO_DEVICE",
 }
 KERNEL_NAMES = ("momentum_cast", "norm", "ns_gram", "ns_poly", "ns_update", "apply", "scale",
-                "adamw", "ns_symmul")
+                "adamw")
 N_KERNELS = len(KERNEL_NAMES)
 
 # Symbols the header declares (checked by the CPU test-suite).
@@ -71,9 +71,7 @@ class _PlanInfo(ctypes.Structure):
     _fields_ = [("n_batches", ctypes.c_int32), ("n_chunks", ctypes.c_int32),
                 ("max_chunk_matrices", ctypes.c_int32), ("matrices", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t), ("ns_algorithmic_flops", ctypes.c_double),
-                ("launches_per_step", ctypes.c_int64), ("ns_performed_flops", ctypes.c_double),
-                ("ns_kind_flops", ctypes.c_double * 4),
-                ("ns_kind_matrix_launches", ctypes.c_int64 * 4)]
+                ("launches_per_step", ctypes.c_int64)]
 
 
 _lib = None
@@ -210,11 +208,7 @@ def muon_plan_describe(groups: Sequence[GroupLike], ns_steps: int = 5,
     info = _PlanInfo()
     _check(load_library().muon_plan_describe(_groups(groups), len(groups), ns_steps,
                                              workspace_bytes_max, ctypes.byref(info)))
-    out = {f: getattr(info, f) for f, _ in _PlanInfo._fields_}
-    kinds = ("ns_gram", "ns_poly", "ns_update", "ns_symmul")
-    out["ns_kind_flops"] = dict(zip(kinds, list(info.ns_kind_flops)))
-    out["ns_kind_matrix_launches"] = dict(zip(kinds, list(info.ns_kind_matrix_launches)))
-    return out
+    return {f: getattr(info, f) for f, _ in _PlanInfo._fields_}
 
 
 def muon_step(handle: int, groups: Sequence[GroupLike], momentum: Sequence, grad: Sequence,

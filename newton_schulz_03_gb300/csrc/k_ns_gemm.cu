@@ -493,24 +493,6 @@ cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float
   return launch<kPoly, kSymBN>(ta, tab, p, grid_cap, stream);
 }
 
-bool ns_symmul_supported(int m) { return use_pairs(m); }
-
-cudaError_t ns_launch_symmul(int m, int count, BatchView L, BatchView R, BatchView C_out, int* err,
-                             int grid_cap, cudaStream_t stream) {
-  if (!use_pairs(m)) return cudaErrorNotSupported;
-  CUtensorMap tl, tl_t, tr, tr_t, tout;
-  const int mn4d = (m % 64 == 0) ? 1 : 0;
-  cudaError_t e = make_map(&tl, L, m, m, count, kBM);
-  if (e == cudaSuccess)
-    e = mn4d ? make_map_mn4d(&tl_t, L, m, m, count, 2) : make_map(&tl_t, L, m, m, count, kBK);
-  if (e == cudaSuccess) e = make_map(&tr, R, m, m, count, kBM);
-  if (e == cudaSuccess)
-    e = mn4d ? make_map_mn4d(&tr_t, R, m, m, count, 2) : make_map(&tr_t, R, m, m, count, kBK);
-  if (e == cudaSuccess) e = make_map_out(&tout, C_out, m, m, count);
-  if (e != cudaSuccess) return e;
-  return ns_pair_symmul(tl, tl_t, tr, tr_t, tout, m, count, C_out, err, grid_cap, stream, mn4d);
-}
-
 cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X, BatchView X_out,
                              const float* inv_norm, int* err, int grid_cap, cudaStream_t stream) {
   CUtensorMap tb, tx;

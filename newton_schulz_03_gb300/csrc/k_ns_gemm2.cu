@@ -78,7 +78,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // tmap_a / tmap_b: K-major boxes (64 x 128); tmap_at / tmap_bt: 64 x 64
   // boxes of the same tensors, for blocks read transposed.
   constexpr bool kSymA = (MODE != kGram);   // A-side source is upper-stored
-  constexpr bool kSymB = (MODE == kPoly || MODE == kSymMul);   // B-side source upper-stored
+  constexpr bool kSymB = (MODE == kPoly);   // B-side source is upper-stored
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -167,13 +167,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           } else {
             ptx::tma_load_3d_pair(sa, &tmap_a, full_leader, kb * kBK, rowA, mat);
           }
-          if (MODE == kUpdate || (kSymB && kblk <= tj)) {
-            // X as the MN-major operand, or a stored block of a symmetric
-            // right-hand operand R read as R[k, j] (MN-major).  The diagonal
-            // block is read this way too, so the product is L R with both
-            // diagonal blocks as stored (their rounding leaves them not quite
-            // symmetric; L R^T there would differ, and the product form of the
-            // iteration amplifies that difference).
+          if (MODE == kUpdate || (kSymB && kblk < tj)) {
+            // X as the MN-major operand, or the transpose of a stored block.
             const CUtensorMap* mb = (MODE == kUpdate) ? &tmap_b : &tmap_bt;
             if (p.mn4d) {
               ptx::tma_load_4d_pair(sb, mb, full_leader, 0, kb * kBK, colB / 64, mat);
@@ -230,7 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < num_kb; ++kb) {
           const int kblk = (kb * kBK) / kPairM;
           const uint32_t a_mn = (kSymA && kblk < ti) ? 1u : 0u;
-          const uint32_t b_mn = (MODE == kUpdate || (kSymB && kblk <= tj)) ? 1u : 0u;
+          const uint32_t b_mn = (MODE == kUpdate || (kSymB && kblk < tj)) ? 1u : 0u;
           const uint32_t idesc = ptx::idesc_bf16_f32(kPairM, kPairN, a_mn, b_mn);
           if (!ptx::mbar_wait_cluster(&full[stage], phase, abort_flag)) {
             ok = false;
@@ -367,7 +362,6 @@ cudaError_t ns_pair_init() {
   if ((e = pair_attr<kGram>()) != cudaSuccess) return e;
   if ((e = pair_attr<kPoly>()) != cudaSuccess) return e;
   if ((e = pair_attr<kUpdate>()) != cudaSuccess) return e;
-  if ((e = pair_attr<kSymMul>()) != cudaSuccess) return e;
   return cudaSuccess;
 }
 
@@ -415,28 +409,6 @@ cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, const C
   p.c2 = a;
   p.err = err;
   return launch_pair<kPoly>(ta, ta_t, ta, ta_t, tout, p, grid_cap, stream);
-}
-
-cudaError_t ns_pair_symmul(const CUtensorMap& tl, const CUtensorMap& tl_t, const CUtensorMap& tr,
-                           const CUtensorMap& tr_t, const CUtensorMap& tout, int m, int count,
-                           BatchView C_out, int* err, int grid_cap, cudaStream_t stream,
-                           int mn4d) {
-  NsArgs p{};
-  p.mn4d = mn4d;
-  p.m = m;
-  p.n = m;
-  p.K = m;
-  p.tiles_m = (m + kPairM - 1) / kPairM;
-  p.tiles_n = p.tiles_m;
-  p.tiles_per_matrix = p.tiles_m * (p.tiles_m + 1) / 2;
-  p.total_tiles = p.tiles_per_matrix * count;
-  p.out_cols = m;
-  p.out = static_cast<__nv_bfloat16*>(const_cast<void*>(C_out.ptr));
-  p.out_ld = C_out.ld;
-  p.out_ms = C_out.ms;
-  p.inv_norm = nullptr;
-  p.err = err;
-  return launch_pair<kSymMul>(tl, tl_t, tr, tr_t, tout, p, grid_cap, stream);
 }
 
 cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,

@@ -70,13 +70,6 @@ cudaError_t ns_launch_update(int m, int n, int count, BatchView B, BatchView X,
                              BatchView X_out, const float* inv_norm, int* err, int grid_cap,
                              cudaStream_t stream);
 
-// C = L R for symmetric m x m L, R that commute (so C is symmetric), both
-// stored as the pair kernels store A and B'; C is stored the same way.
-// CTA-pair path only: ns_symmul_supported(m) says whether m takes it.
-bool ns_symmul_supported(int m);
-cudaError_t ns_launch_symmul(int m, int count, BatchView L, BatchView R, BatchView C_out, int* err,
-                             int grid_cap, cudaStream_t stream);
-
 // ------------------------------------------------------------------ AdamW
 constexpr int kAdamwMaxTensors = 40;
 // Tensors of one AdamW launch, passed by value in the kernel parameters.
@@ -118,10 +111,6 @@ cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, const C
 cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const CUtensorMap& tx,
                            const CUtensorMap& tout, int m, int n, int count, BatchView X_out,
                            const float* inv_norm, int* err, int grid_cap, cudaStream_t stream,
-                           int mn4d);
-cudaError_t ns_pair_symmul(const CUtensorMap& tl, const CUtensorMap& tl_t, const CUtensorMap& tr,
-                           const CUtensorMap& tr_t, const CUtensorMap& tout, int m, int count,
-                           BatchView C_out, int* err, int grid_cap, cudaStream_t stream,
                            int mn4d);
 
 // Record `msg` as the calling thread's last error text and return `status`

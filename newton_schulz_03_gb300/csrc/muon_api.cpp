@@ -18,7 +18,6 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -62,35 +61,13 @@ int64_t max_count_per_launch(int m, int n) {
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-// Product form of the iteration for wide batches.  Every B'_k = a I + b A_k
-// + c A_k^2 is a polynomial in A_0 = X_0 X_0^T, so all of them commute with
-// each other and with every A_k, and
-//   A_{k+1} = X_{k+1} X_{k+1}^T = B'_k A_k B'_k = (B'_k A_k) B'_k,
-//   X_N     = B'_{N-1} ... B'_1 B'_0 X_0 = Q X_0.
-// After the first Gram matrix the iteration runs on m x m symmetric
-// products only (per matrix 3 m^2 n + (4N - 3) m^3 flops instead of
-// N (3 m^2 n + m^3)) and X is multiplied once, at the end.  Used for
-// n >= 2.5 m on the CTA-pair path with N >= 2; MUON_NS_PRODUCT=0 turns it
-// off.  (Closer to square the rounding of the m x m products is amplified
-// by the polynomial: at n = 1.25 m the error against the exact iteration
-// is ~2e-2, at n >= 2 m within ~20% of the per-iteration form's.)
-bool use_product_form(int m, int n) {
-  static const bool on = [] {
-    const char* v = std::getenv("MUON_NS_PRODUCT");
-    return !(v != nullptr && std::strcmp(v, "0") == 0);
-  }();
-  return on && muon::ns_symmul_supported(m) && 2 * int64_t(n) >= 5 * int64_t(m);
-}
-
 int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
 
 // Workspace layout of one chunk of `cap` matrices of wide shape m x n.
 struct ChunkLayout {
   int64_t ldx, ldm;  // row pitches (elements) of X and of A/B
   int tiles;         // elementwise tiles per matrix (norm partials)
-  bool product;      // product form: two more m x m buffers (C, D)
-  size_t off_x0, off_x1, off_a, off_b, off_c, off_d, off_part, off_inv, bytes;
+  size_t off_x0, off_x1, off_a, off_b, off_part, off_inv, bytes;
 };
 
 ChunkLayout chunk_layout(int m, int n, int64_t cap) {
@@ -105,9 +82,6 @@ ChunkLayout chunk_layout(int m, int n, int64_t cap) {
   L.off_x1 = off; off += xb;
   L.off_a = off; off += ab;
   L.off_b = off; off += ab;
-  L.product = use_product_form(m, n);
-  L.off_c = off; off += L.product ? ab : 0;
-  L.off_d = off; off += L.product ? ab : 0;
   L.off_part = off; off += align_up(size_t(cap) * L.tiles * 4, kAlign);
   L.off_inv = off; off += align_up(size_t(cap) * 4, kAlign);
   L.bytes = off;
@@ -116,8 +90,7 @@ ChunkLayout chunk_layout(int m, int n, int64_t cap) {
 
 size_t per_matrix_bytes(int m, int n) {
   const int64_t ldx = pad8(n), ldm = pad8(m);
-  const int sq = use_product_form(m, n) ? 4 : 2;   // A, B' (and C, D)
-  return size_t(2) * m * ldx * 2 + size_t(sq) * m * ldm * 2 +
+  return size_t(2) * m * ldx * 2 + size_t(2) * m * ldm * 2 +
          size_t(muon::ew_tiles_per_matrix(m, n)) * 4 + 4;
 }
 
@@ -141,9 +114,6 @@ struct Plan {
   int64_t matrices = 0;
   size_t ws_bytes = 0;
   double flops = 0.0;
-  double flops_performed = 0.0;
-  double kind_flops[4] = {0, 0, 0, 0};              // gram, square, update, symmetric product
-  int64_t kind_matrix_launches[4] = {0, 0, 0, 0};
   int64_t launches = 0;
 };
 
@@ -202,22 +172,6 @@ muon_status_t build_plan(const muon_group_t* groups, int32_t n_groups, int32_t n
     P.ws_bytes = std::max(P.ws_bytes, chunk_layout(m, n, cap).bytes);
     P.matrices += total;
     P.flops += double(total) * ns_steps * (3.0 * m * double(m) * n + double(m) * m * m);
-    {
-      // Launches per matrix of each class, and their flops.
-      const double gram = double(m) * m * n, sq = double(m) * m * m, upd = 2.0 * gram;
-      int64_t per[4] = {ns_steps, ns_steps, ns_steps, 0};
-      if (ns_steps >= 2 && use_product_form(m, n)) {
-        per[0] = 1;
-        per[2] = 1;
-        per[3] = 3 * (ns_steps - 1);
-      }
-      const double f[4] = {gram, sq, upd, sq};
-      for (int k = 0; k < 4; ++k) {
-        P.kind_flops[k] += double(total) * per[k] * f[k];
-        P.kind_matrix_launches[k] += total * per[k];
-        P.flops_performed += double(total) * per[k] * f[k];
-      }
-    }
     // Cut the batch into chunks of at most `cap` matrices.
     Chunk cur{m, n, 0, {}};
     for (int g : b.second) {
@@ -237,9 +191,7 @@ muon_status_t build_plan(const muon_group_t* groups, int32_t n_groups, int32_t n
   }
   for (const Chunk& c : P.chunks) {
     P.max_chunk = std::max(P.max_chunk, c.count);
-    const bool prod = ns_steps >= 2 && use_product_form(c.m, c.n);
-    P.launches += 2 * static_cast<int64_t>(c.segs.size()) + 1 +
-                  (prod ? 4 * ns_steps - 1 : (ns_steps > 0 ? 3 * ns_steps : 1));
+    P.launches += 2 * static_cast<int64_t>(c.segs.size()) + 1 + (ns_steps > 0 ? 3 * ns_steps : 1);
   }
   *plan = std::move(P);
   return MUON_OK;
@@ -340,62 +292,10 @@ struct Coeffs {
 // ns_steps iterations on `count` wide matrices.  Reads x (never written);
 // iteration k writes dst[k]; the last one lands in `out`.  A, B: scratch.
 // `sched` holds the (a, b, c) of every iteration (at least `steps` entries).
-// The product form (see use_product_form): A_0 = alpha X_0 X_0^T, then per
-// iteration k: B'_k = p_k(A_k); Q_k = B'_k Q_{k-1} (Q_0 = B'_0); and for
-// k < N - 1, A_{k+1} = (B'_k A_k) B'_k; finally X_N = alpha Q_{N-1} X_0.
-// P[0..2] rotate through the roles B'_k, Q and the scratch (B'_k A_k).
-muon_status_t run_newton_schulz_product(muon_handle_t h, int m, int n, int count,
-                                        muon::BatchView x, muon::BatchView out, muon::BatchView A,
-                                        const muon::BatchView* P, const float* inv_norm,
-                                        int steps, const Coeffs* sched, cudaStream_t s) {
-  cudaError_t e;
-  auto sym = [&](const muon::BatchView& L, const muon::BatchView& R, const muon::BatchView& C) {
-    LaunchScope Ls(h, MUON_KERNEL_NS_SYMMUL, s);
-    return muon::ns_launch_symmul(m, count, L, R, C, h->dev_err, h->num_sms, s);
-  };
-  auto poly = [&](int k, const muon::BatchView& B) {
-    LaunchScope Ls(h, MUON_KERNEL_NS_POLY, s);
-    const Coeffs co = sched[k];
-    return muon::ns_launch_poly(m, count, A, B, co.a, co.b, co.c, h->dev_err, h->num_sms, s);
-  };
-  {
-    LaunchScope Ls(h, MUON_KERNEL_NS_GRAM, s);
-    e = muon::ns_launch_gram(m, n, count, x, A, inv_norm, h->dev_err, h->num_sms, s);
-  }
-  if (e == cudaSuccess) e = poly(0, P[0]);
-  int q = 0, c = 1;                                    // Q_0 = B'_0 in P[0]
-  if (e == cudaSuccess) e = sym(P[0], A, P[1]);        // B'_0 A_0
-  if (e == cudaSuccess) e = sym(P[1], P[0], A);        // A_1
-  for (int k = 1; k < steps && e == cudaSuccess; ++k) {
-    const int b = c;                                   // the scratch is free again
-    const int qn = 3 - b - q;
-    e = poly(k, P[b]);                                 // B'_k
-    if (e == cudaSuccess) e = sym(P[b], P[q], P[qn]);  // Q_k = B'_k Q_{k-1}
-    if (e == cudaSuccess && k < steps - 1) {
-      c = q;                                           // Q_{k-1} is free
-      e = sym(P[b], A, P[c]);                          // B'_k A_k
-      if (e == cudaSuccess) e = sym(P[c], P[b], A);    // A_{k+1}
-    }
-    q = qn;
-  }
-  if (e == cudaSuccess) {
-    LaunchScope Ls(h, MUON_KERNEL_NS_UPDATE, s);
-    e = muon::ns_launch_update(m, n, count, P[q], x, out, inv_norm, h->dev_err, h->num_sms, s);
-  }
-  if (e != cudaSuccess)
-    return fail(MUON_ERR_CUDA, "Newton-Schulz launch: %s %s", cudaGetErrorString(e),
-                muon::ns_last_encode_error());
-  return MUON_OK;
-}
-
-// P2, P3: two more m x m buffers for the product form (ptr NULL: the
-// iteration runs one Gram, square and update product per step).  With the
-// product form the result goes to `out`, which must not be `x`.
 muon_status_t run_newton_schulz(muon_handle_t h, int m, int n, int count, muon::BatchView x,
                                 muon::BatchView out, muon::BatchView other, muon::BatchView A,
-                                muon::BatchView B, muon::BatchView P2, muon::BatchView P3,
-                                const float* inv_norm, int steps, const Coeffs* sched,
-                                cudaStream_t s) {
+                                muon::BatchView B, const float* inv_norm, int steps,
+                                const Coeffs* sched, cudaStream_t s) {
   if (steps == 0) {
     LaunchScope L(h, MUON_KERNEL_SCALE, s);
     cudaError_t e = muon::launch_scale_bf16(
@@ -403,10 +303,6 @@ muon_status_t run_newton_schulz(muon_handle_t h, int m, int n, int count, muon::
         static_cast<uint16_t*>(const_cast<void*>(out.ptr)), out.ld, out.ms, inv_norm, s);
     if (e != cudaSuccess) return cuda_fail(e, "scale kernel launch");
     return MUON_OK;
-  }
-  if (steps >= 2 && P2.ptr != nullptr && P3.ptr != nullptr) {
-    const muon::BatchView P[3] = {B, P2, P3};
-    return run_newton_schulz_product(h, m, n, count, x, out, A, P, inv_norm, steps, sched, s);
   }
   muon::BatchView src = x;
   for (int k = 0; k < steps; ++k) {
@@ -575,11 +471,6 @@ muon_status_t muon_plan_describe(const muon_group_t* groups, int32_t n_groups, i
   out->workspace_bytes = P.ws_bytes;
   out->ns_algorithmic_flops = P.flops;
   out->launches_per_step = P.launches;
-  out->ns_performed_flops = P.flops_performed;
-  for (int k = 0; k < 4; ++k) {
-    out->ns_kind_flops[k] = P.kind_flops[k];
-    out->ns_kind_matrix_launches[k] = P.kind_matrix_launches[k];
-  }
   return MUON_OK;
 }
 
@@ -666,15 +557,11 @@ muon_status_t step_impl(muon_handle_t h, const muon_group_t* groups, int32_t n_g
     }
     // The iterates alternate between x0 and x1, starting from x0; the
     // final one lands in x0 for an even (non-zero) step count, else in x1.
-    // The product form writes its single result to x1.
-    const bool product = L.product && ns_steps >= 2;
-    uint16_t* fin = (!product && ns_steps > 0 && ns_steps % 2 == 0) ? x0 : x1;
+    uint16_t* fin = (ns_steps > 0 && ns_steps % 2 == 0) ? x0 : x1;
     uint16_t* oth = (fin == x0) ? x1 : x0;
     const muon::BatchView vx0{x0, L.ldx, xms}, vfin{fin, L.ldx, xms}, voth{oth, L.ldx, xms};
     const muon::BatchView vA{A, L.ldm, ams}, vB{B, L.ldm, ams};
-    const muon::BatchView vC{product ? ws + L.off_c : nullptr, L.ldm, ams};
-    const muon::BatchView vD{product ? ws + L.off_d : nullptr, L.ldm, ams};
-    st = run_newton_schulz(h, c.m, c.n, c.count, vx0, vfin, voth, vA, vB, vC, vD, inv, ns_steps,
+    st = run_newton_schulz(h, c.m, c.n, c.count, vx0, vfin, voth, vA, vB, inv, ns_steps,
                            o.sched.data(), s);
     if (st != MUON_OK) return st;
     for (const Segment& sg : c.segs) {
@@ -972,17 +859,13 @@ muon_status_t muon_newton_schulz_bf16(muon_handle_t h, int32_t m, int32_t n, int
   const size_t xbytes = size_t(count) * m * n * 2;
   const uintptr_t xb = reinterpret_cast<uintptr_t>(x), ob = reinterpret_cast<uintptr_t>(out);
   if (xb < ob + xbytes && ob < xb + xbytes) return fail(MUON_ERR_INVALID_ARG, "x and out overlap");
-  // Scratch: one more X buffer and A, B (and C for the Gram recurrence) --
-  // in chunks that fit the cap.
-  const bool product = use_product_form(m, n) && ns_steps >= 2;
-  const int nsq = product ? 4 : 2;
-  const size_t pm = align_up(size_t(m) * n * 2, 16) + nsq * align_up(size_t(m) * m * 2, 16);
+  // Scratch: one more X buffer and A, B -- in chunks that fit the cap.
+  const size_t pm = align_up(size_t(m) * n * 2, 16) + 2 * align_up(size_t(m) * m * 2, 16);
   int64_t cap = static_cast<int64_t>(h->ws_cap / pm);
   if (cap < 1) cap = 1;
   if (cap > count) cap = count;
   cap = std::min(cap, max_count_per_launch(m, n));
-  const size_t need = align_up(size_t(cap) * m * n * 2, kAlign) +
-                     nsq * align_up(size_t(cap) * m * m * 2, kAlign);
+  const size_t need = align_up(size_t(cap) * m * n * 2, kAlign) + 2 * align_up(size_t(cap) * m * m * 2, kAlign);
   st = ensure_workspace(h, need);
   if (st != MUON_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(h->ws);
@@ -990,20 +873,13 @@ muon_status_t muon_newton_schulz_bf16(muon_handle_t h, int32_t m, int32_t n, int
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + align_up(size_t(cap) * m * n * 2, kAlign));
   uint16_t* B = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(A) +
                                             align_up(size_t(cap) * m * m * 2, kAlign));
-  uint16_t* Cm = product ? reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(B) +
-                                                       align_up(size_t(cap) * m * m * 2, kAlign))
-                         : nullptr;
-  uint16_t* Dm = product ? reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(Cm) +
-                                                       align_up(size_t(cap) * m * m * 2, kAlign))
-                         : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t xms = int64_t(m) * n, ams = int64_t(m) * m;
   for (int64_t done = 0; done < count; done += cap) {
     const int take = static_cast<int>(std::min<int64_t>(count - done, cap));
     const muon::BatchView vx{x + done * xms, n, xms}, vo{out + done * xms, n, xms};
-    const muon::BatchView vt{other, n, xms}, vA{A, m, ams}, vB{B, m, ams}, vC{Cm, m, ams},
-        vD{Dm, m, ams};
-    st = run_newton_schulz(h, m, n, take, vx, vo, vt, vA, vB, vC, vD, inv_norm + done, ns_steps,
+    const muon::BatchView vt{other, n, xms}, vA{A, m, ams}, vB{B, m, ams};
+    st = run_newton_schulz(h, m, n, take, vx, vo, vt, vA, vB, inv_norm + done, ns_steps,
                            sched.data(), s);
     if (st != MUON_OK) return st;
   }

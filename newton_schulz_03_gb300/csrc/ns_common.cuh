@@ -15,10 +15,7 @@
 namespace muon {
 namespace nsk {
 
-// kSymMul: C = L R for two upper-stored symmetric m x m operands whose
-// product is symmetric (they commute: the next Gram matrix B' A B' of the
-// iteration, see run_newton_schulz); plain epilogue.
-enum NsMode : int { kGram = 0, kPoly = 1, kUpdate = 2, kSymMul = 3 };
+enum NsMode : int { kGram = 0, kPoly = 1, kUpdate = 2 };
 
 constexpr int kBM = 128;   // accumulator rows per CTA (TMEM lanes)
 constexpr int kBK = 64;    // K per pipeline stage: one 128-byte swizzle row of BF16

@@ -126,23 +126,3 @@ def test_missing_library_fails_loudly(tmp_path):
                        text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.startswith("raised") and "is missing" in r.stdout
-
-
-def test_plan_product_form_accounting(lib):
-    """Wide batches on the CTA-pair path (n >= 2.5 m, m > 128, ns_steps >= 2)
-    run the product form: 3 m^2 n + (4N - 3) m^3 flops per matrix and
-    4N - 1 Newton-Schulz launches; the plan reports both flop counts."""
-    sq = lib.muon_plan_describe([(2048, 2048, 4)], ns_steps=5)
-    assert sq["ns_performed_flops"] == sq["ns_algorithmic_flops"]
-    assert sq["launches_per_step"] == 1 + 1 + 15 + 1
-    m, n, k = 1536, 4096, 8
-    wide = lib.muon_plan_describe([(m, n, k)], ns_steps=5)
-    assert wide["ns_performed_flops"] == pytest.approx(k * (3.0 * m * m * n + 17.0 * m ** 3))
-    assert wide["ns_algorithmic_flops"] == pytest.approx(k * 5 * (3.0 * m * m * n + m ** 3))
-    assert wide["launches_per_step"] == 1 + 1 + 19 + 1
-    one = lib.muon_plan_describe([(m, n, k)], ns_steps=1)
-    assert one["ns_performed_flops"] == one["ns_algorithmic_flops"]
-    # Narrower than 2.5 m, or m <= 128: the per-iteration form.
-    for g in ([(1024, 2048, 2)], [(128, 1024, 2)]):
-        d = lib.muon_plan_describe(g, ns_steps=5)
-        assert d["ns_performed_flops"] == d["ns_algorithmic_flops"]

@@ -237,42 +237,6 @@ def test_step_chunked_workspace(ns, ):
         run_step_and_check(ns, hh.value, [(r, c, k)], arrays)
 
 
-@pytest.mark.parametrize("m,n,count,steps", [(256, 1024, 3, 5), (392, 1000, 2, 5),
-                                             (512, 1280, 2, 5), (256, 768, 2, 2),
-                                             (256, 768, 2, 4)])
-def test_product_form_path(ns, h, m, n, count, steps):
-    """Wide batches (n >= 2.5 m) on the CTA-pair path run the product form:
-    one Gram matrix X X^T, then per iteration the square product and
-    symmetric m x m products (Q = B'_k Q, A = (B'_k A) B'_k), and one final
-    X_N = Q X_0.  The launches show it (even step counts included: the
-    result must not land on the input), and the result matches the oracle."""
-    rng = np.random.default_rng(m + n + steps)
-    Xb = o.bf16_rne_bits(rng.standard_normal((count, m, n), dtype=np.float32))
-    Xf = o.bf16_bits_to_f64(Xb)
-    inv = np.array([1.0 / (np.linalg.norm(Xf[i]) + o.NORM_EPS) for i in range(count)],
-                   dtype=np.float32)
-    out = torch.zeros((count, m, n), dtype=torch.int16, device="cuda")
-    ns.muon_reset_kernel_stats(h)
-    ns.muon_newton_schulz_bf16(h, m, n, count, dev(Xb.view(np.int16)), out, dev(inv), steps)
-    ns.muon_last_device_error(h)
-    st = ns.muon_kernel_stats(h)["launches"]
-    assert (st["ns_gram"], st["ns_poly"], st["ns_symmul"], st["ns_update"]) == \
-        (1, steps, 3 * (steps - 1), 1)
-    got = o.bf16_bits_to_f64(u16(out))
-    for i in range(count):
-        ref = o.newton_schulz(Xf[i], 1.0 / float(inv[i]), steps)
-        assert rel_fro(got[i], ref) <= NS_TOL
-
-
-def test_product_form_step_even_steps(ns, h):
-    """muon_step with the product form and an even step count (the
-    per-iteration form would end in the input buffer)."""
-    rng = np.random.default_rng(17)
-    r, c, k = 1024, 256, 3                # tall: runs as 256 x 1024
-    arrays = [tuple(rng.standard_normal((k, r, c), dtype=np.float32) for _ in range(3)) + (1.0,)]
-    run_step_and_check(ns, h, [(r, c, k)], arrays, steps=4)
-
-
 def test_step_host_buffers(ns, h):
     rng = np.random.default_rng(11)
     r, c, k = 192, 96, 3

@@ -62,9 +62,7 @@ def check(arrays, Wg, Mg, groups, steps, coeffs, nesterov, rule):
             assert (dw - fp) / (LR * scale * on) <= NS_TOL
 
 
-# (640, 256): a tall group that runs as 256 x 640 (n = 2.5 m) in the product
-# form of the iteration, so the variants are checked on both forms.
-SHAPES = [(128, 320, 2), (384, 256, 2), (64, 128, 3), (640, 256, 2)]
+SHAPES = [(128, 320, 2), (384, 256, 2), (64, 128, 3)]
 
 
 def test_nesterov(ns, h):
