@@ -154,8 +154,9 @@ def test_extreme_momentum_scales(ns, h, scale):
         assert np.max(np.abs(Xg)) < 4.0      # the working copy was brought to unit scale
 
 
-@pytest.mark.parametrize("rank", [1, 5, 20])
-def test_rank_deficient_momentum(ns, h, rank):
+@pytest.mark.parametrize("m,n,rank", [(256, 384, 1), (256, 384, 5), (256, 384, 20),
+                                      (256, 1024, 1), (256, 1024, 5), (512, 2048, 3)])
+def test_rank_deficient_momentum(ns, h, m, n, rank):
     """A rank-r momentum: BF16 rounding of X puts noise in the null space,
     which the quintic amplifies (~a^5 = 480x), so even a BF16 emulation that
     rounds at exactly the GPU's points differs from the exact iteration by
@@ -163,8 +164,8 @@ def test_rank_deficient_momentum(ns, h, rank):
     kernels.  What the method fixes is the output on the input's signal
     subspace, U_r^T O V_r, and the bound sigma(O) <= 1.2024 of the
     polynomial's band; both are checked against the oracle."""
-    m, n, count = 256, 384, 2
-    rng = np.random.default_rng(300 + rank)
+    count = 2
+    rng = np.random.default_rng(300 + rank + n)
     for i in range(count):
         M = (rng.standard_normal((m, rank)) @ rng.standard_normal((rank, n))).astype(np.float32)
         Xb = o.bf16_rne_bits(M)
@@ -182,3 +183,35 @@ def test_rank_deficient_momentum(ns, h, rank):
         err = np.linalg.norm(pg - pr) / np.linalg.norm(pr)
         assert err <= 2e-2, f"rank {rank}: signal-subspace error {err:.3e}"
         assert np.linalg.svd(Og, compute_uv=False)[0] <= 1.2024 * (1 + 2.0**-7)
+
+
+def test_low_rank_expert_in_a_batch(ns, h):
+    """An MoE expert that received two tokens has a rank-2 gradient; with
+    zero momentum its orthogonalised update must still have singular values
+    inside the band and match the oracle on its signal subspace, next to
+    full-rank experts of the same batch (which must match as usual)."""
+    r, c, k = 512, 2048, 6
+    rng = np.random.default_rng(2024)
+    W = rng.standard_normal((k, r, c), dtype=np.float32)
+    M = rng.standard_normal((k, r, c), dtype=np.float32) * np.float32(1e-3)
+    G = rng.standard_normal((k, r, c), dtype=np.float32) * np.float32(1e-3)
+    tok_in, tok_out = rng.standard_normal((r, 2)), rng.standard_normal((2, c))
+    G[3] = (tok_in @ tok_out).astype(np.float32) * np.float32(1e-3)
+    M[3] = 0.0
+    dW, dM, dG = (torch.from_numpy(a.copy()).cuda() for a in (W, M, G))
+    ns.muon_step(h, [(r, c, k)], [dM], [dG], [dW], LR, WD, MU, STEPS)
+    ns.muon_last_device_error(h)
+    Wg = dW.cpu().numpy()
+    for i in range(k):
+        st = o.muon_step_matrix(W[i], M[i], G[i], lr=LR, wd=WD, mu=MU, ns_steps=STEPS)
+        if i != 3:
+            assert update_error(Wg[i], st, W[i]) <= 2e-2
+            continue
+        # the kernel's decay, fmaf(-lr, wd, 1) rounded once to FP32
+        decay = np.float64(np.float32(1.0 - np.float64(np.float32(LR)) * np.float64(np.float32(WD))))
+        Og = (W[i].astype(np.float64) * decay - Wg[i].astype(np.float64)) / LR
+        assert np.linalg.svd(Og, compute_uv=False)[0] <= 1.2024 * 1.01
+        U, _, Vt = np.linalg.svd(G[i].astype(np.float64), full_matrices=False)
+        Ur, Vr = U[:, :2], Vt[:2].T
+        pg, pr = Ur.T @ Og @ Vr, Ur.T @ st.O @ Vr
+        assert np.linalg.norm(pg - pr) / np.linalg.norm(pr) <= 2e-2
