@@ -342,6 +342,38 @@ def test_emulated_bf16_mode_is_close_to_exact():
     assert 1e-4 < err < 2e-2
 
 
+def test_error_model_check_detects_rounding_mistakes():
+    # The GPU parity tests require the kernels' error against the exact
+    # iteration to match the emulation's (rounding where the kernels store)
+    # within 15% + 5e-4.  Mistakes planted here, in a copy of the emulated
+    # iteration on the CPU -- one extra BF16 rounding of c A^2, or rounding
+    # before the a I term is added -- stay under the plain 2e-2 bar but
+    # fail that check.
+    rng = np.random.default_rng(52)
+    X = o.bf16_rne(rng.standard_normal((128, 256)).astype(np.float32))
+    s = np.linalg.norm(X) + o.NORM_EPS
+    ref = o.newton_schulz(X, s)
+    model = rel(o.newton_schulz(X, s, emulate_bf16=True), ref)
+    rnd = o._round_bf16_any
+    a, b, c = o.NS_COEFFS
+
+    def planted(kind):
+        Y = X / s
+        for _ in range(5):
+            A = rnd(Y @ Y.T)
+            eye = np.eye(A.shape[0])
+            if kind == "extra_round":
+                B = rnd(b * A + rnd(c * (A @ A)) + a * eye)
+            else:
+                B = rnd(rnd(b * A + c * (A @ A)) + a * eye)
+            Y = rnd(B @ Y)
+        return Y
+
+    for kind in ("extra_round", "early_round"):
+        err = rel(planted(kind), ref)
+        assert err <= 2e-2 and err > 1.15 * model + 5e-4, (kind, err, model)
+
+
 def test_emulated_bf16_floor_on_rank_deficient_input():
     # Rank-1 input: BF16 rounding puts noise in the null space that the
     # quintic amplifies, so the emulation (rounding where the GPU stores)
