@@ -244,6 +244,17 @@ def test_step_chunked_workspace(ns, ):
         run_step_and_check(ns, hh.value, [(r, c, k)], arrays)
 
 
+@pytest.mark.parametrize("steps", [0, 1, 2, 4])
+@pytest.mark.parametrize("r,c", [(384, 256), (96, 160)])
+def test_step_iteration_counts(ns, h, steps, r, c):
+    """muon_step with 0 (the normalised momentum), 1, 2 and 4 iterations: the
+    final iterate lands in the buffer the apply kernel reads, on the
+    CTA-pair path (m > 128) and the single-CTA path."""
+    rng = np.random.default_rng(100 * steps + r)
+    arrays = [tuple(rng.standard_normal((2, r, c), dtype=np.float32) for _ in range(3)) + (1.0,)]
+    run_step_and_check(ns, h, [(r, c, 2)], arrays, steps=steps)
+
+
 def test_step_host_buffers(ns, h):
     rng = np.random.default_rng(11)
     r, c, k = 192, 96, 3
