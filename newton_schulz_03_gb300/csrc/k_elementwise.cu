@@ -8,9 +8,10 @@
 //  * norm_finalize: deterministic per-matrix reduction of the partials.
 //  * apply_update: "cast the update back to FP32 and apply it to the
 //    weights" (same section, resharding step 5) with decoupled weight decay.
-//    Traffic: read W, O; write W.  Tall matrices (O transposed back through
-//    shared memory) and padded update pitches use 64 x 64 tiles; the
-//    contiguous case streams both arrays flat.
+//    Traffic: read W, O; write W.  The contiguous wide case streams both
+//    arrays flat; tall matrices (O transposed back through shared memory)
+//    run on a resident grid with the next tile's O prefetched; unaligned
+//    update pitches fall back to one 64 x 64 tile per block.
 //  * scale_bf16: the degenerate zero-iteration case O = X / s.
 //
 // Except the flat apply, they work on 64 x 64 tiles of the source matrix
@@ -18,6 +19,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "kernels.h"
@@ -294,6 +296,114 @@ __global__ void __launch_bounds__(kThreads) apply_update_kernel(
   }
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_prior() {   // all groups but the newest
+  asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+}
+
+// Apply for a tall batch (rows > cols; O stored wide, cols x rows).  A grid
+// of resident blocks walks tiles of 128 W rows x 64 W columns; while a
+// block updates one tile, the O block of its next tile (64 O rows x 256
+// bytes) is already on its way into the other half of a double buffer
+// (cp.async, 16 bytes per copy), so the O reads never wait behind the W
+// traffic.  The 16-byte chunk q of buffer row j sits at chunk
+// q ^ ((j >> 2) & 7): the update reads one O element of each of 16 rows
+// j = 4k + e at a time, which without the swizzle share two banks.
+// Needs cols % 4 == 0, W 16-byte aligned, O pitches multiples of 8
+// elements and O 16-byte aligned.
+constexpr int kTallR = 128;   // W rows per tile (= O columns)
+
+__device__ __forceinline__ int tall_chunk(int j, int q) { return q ^ ((j >> 2) & 7); }
+
+__global__ void __launch_bounds__(kThreads) apply_update_tall_kernel(
+    int rows, int cols, int count, float* __restrict__ W, const uint16_t* __restrict__ O,
+    int64_t o_ld, int64_t o_ms, float lr, float wd, float scale) {
+  grid_dep_wait();    // inputs come from the previous kernel of the step
+  grid_dep_launch();
+  __shared__ __align__(16) uint16_t sO[2][T][kTallR];
+  const int tiles_c = (cols + T - 1) / T;
+  const int per_matrix = ((rows + kTallR - 1) / kTallR) * tiles_c;
+  const int64_t total = static_cast<int64_t>(per_matrix) * count;
+  const float decay = fmaf(-lr, wd, 1.0f);
+  const float step = lr * scale;
+
+  // O block of tile t: O rows tc*64.. (W columns), O columns tr*128.. (W rows).
+  auto stage = [&](int64_t t, int buf) {
+    const int64_t mat = t / per_matrix;
+    const int l = static_cast<int>(t - mat * per_matrix);
+    const int tr = l / tiles_c, tc = l - (l / tiles_c) * tiles_c;
+    const uint16_t* Om = O + mat * o_ms;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = threadIdx.x + kThreads * j;   // 0..1023
+      const int orow_l = idx >> 4;                  // 0..63
+      const int q = idx & 15;                       // 16-byte chunk of the row
+      const int orow = tc * T + orow_l;
+      const int ocol = tr * kTallR + q * 8;
+      if (orow >= cols) continue;
+      uint16_t* dst = &sO[buf][orow_l][tall_chunk(orow_l, q) * 8];
+      const uint16_t* src = Om + static_cast<int64_t>(orow) * o_ld + ocol;
+      if (ocol + 7 < rows) {
+        cp_async16(dst, src);
+      } else {
+        for (int e = 0; e < 8; ++e) dst[e] = (ocol + e < rows) ? src[e] : 0;
+      }
+    }
+  };
+
+  const int rr = threadIdx.x >> 4;        // 0..15
+  const int cc = (threadIdx.x & 15) * 4;  // 0..60
+  int buf = 0;
+  int64_t t = blockIdx.x;
+  if (t < total) stage(t, 0);
+  cp_async_commit();
+  for (; t < total; t += gridDim.x) {
+    const int64_t tn = t + gridDim.x;
+    if (tn < total) stage(tn, buf ^ 1);
+    cp_async_commit();
+    const int64_t mat = t / per_matrix;
+    const int l = static_cast<int>(t - mat * per_matrix);
+    const int tr = l / tiles_c, tc = l - (l / tiles_c) * tiles_c;
+    float* Wm = W + mat * static_cast<int64_t>(rows) * cols;
+    const int c = tc * T + cc;
+    float4 w[kTallR / 16];
+#pragma unroll
+    for (int i = 0; i < kTallR / 16; ++i) {
+      const int r = tr * kTallR + rr + 16 * i;
+      if (r < rows && c < cols)
+        w[i] = *reinterpret_cast<const float4*>(Wm + static_cast<int64_t>(r) * cols + c);
+    }
+    cp_async_wait_prior();   // this tile's O block has landed (the next may still fly)
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTallR / 16; ++i) {
+      const int lr_ = rr + 16 * i;   // O column within the block
+      const int r = tr * kTallR + lr_;
+      if (r < rows && c < cols) {
+        const int q = lr_ >> 3, e8 = lr_ & 7;
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[e] = bf16_to_f32(sO[buf][cc + e][tall_chunk(cc + e, q) * 8 + e8]);
+        float4 v = w[i];
+        v.x = fmaf(v.x, decay, -step * o[0]);
+        v.y = fmaf(v.y, decay, -step * o[1]);
+        v.z = fmaf(v.z, decay, -step * o[2]);
+        v.w = fmaf(v.w, decay, -step * o[3]);
+        *reinterpret_cast<float4*>(Wm + static_cast<int64_t>(r) * cols + c) = v;
+      }
+    }
+    __syncthreads();   // sO[buf] is refilled by the iteration after next
+    buf ^= 1;
+  }
+}
+
 // Apply for a wide (or square) batch whose update has the weights' own
 // pitch: W and O are then flat arrays of the same length, and a grid-stride
 // loop over 4-element groups (float4 of W, 8 bytes of O) streams them with
@@ -336,6 +446,21 @@ __global__ void __launch_bounds__(kThreads) scale_bf16_kernel(
 
 }  // namespace
 
+// Multiprocessor count of the current device (grid sizing of the
+// grid-stride kernels).
+static int sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      sms = v;
+    else
+      return 148;
+  }
+  return sms;
+}
+
 cudaError_t launch_momentum_cast(int rows, int cols, int count, float* M, const float* G,
                                  float mu, uint16_t* X, int64_t x_ld, int64_t x_ms,
                                  float* partials, cudaStream_t stream, bool nesterov) {
@@ -362,17 +487,23 @@ cudaError_t launch_apply_update(int rows, int cols, int count, float* W, const u
   if (count <= 0) return cudaSuccess;
   if (rows <= cols && o_ld == cols && o_ms == int64_t(rows) * cols && (cols & 3) == 0 &&
       (reinterpret_cast<uintptr_t>(W) & 15) == 0 && (reinterpret_cast<uintptr_t>(O) & 7) == 0) {
-    static int sms = 0;
-    if (sms == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 148;
-    }
     const int64_t n4 = int64_t(count) * rows * cols / 4;
-    return launch_pdl(apply_update_flat_kernel, dim3(sms * 8), dim3(kThreads), 0, stream, n4,
+    return launch_pdl(apply_update_flat_kernel, dim3(sm_count() * 8), dim3(kThreads), 0, stream, n4,
                       reinterpret_cast<float4*>(W), reinterpret_cast<const uint2*>(O), lr, wd,
                       scale);
+  }
+  if (rows > cols && (cols & 3) == 0 && (o_ld & 7) == 0 && (o_ms & 7) == 0 &&
+      (reinterpret_cast<uintptr_t>(W) & 15) == 0 && (reinterpret_cast<uintptr_t>(O) & 15) == 0) {
+    const int64_t tiles =
+        int64_t((rows + kTallR - 1) / kTallR) * ((cols + T - 1) / T) * count;
+    static int resident = 0;   // blocks of this kernel one SM holds at once
+    if (resident == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                              &resident, apply_update_tall_kernel, kThreads, 0) != cudaSuccess ||
+                          resident < 1))
+      resident = 1;
+    const int64_t grid = std::min<int64_t>(tiles, int64_t(sm_count()) * resident);
+    return launch_pdl(apply_update_tall_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                      0, stream, rows, cols, count, W, O, o_ld, o_ms, lr, wd, scale);
   }
   const dim3 grid(ew_tiles_per_matrix(rows, cols), count);
   auto kern = rows > cols ? apply_update_kernel<true> : apply_update_kernel<false>;

@@ -83,7 +83,10 @@ def test_momentum_cast(ns, h, rows, cols, count):
 
 # ----------------------------------------------------------------- step 5
 @pytest.mark.parametrize("rows,cols,count", [
-    (128, 64, 4), (64, 128, 3), (200, 136, 2), (37, 5, 2), (1, 40, 3), (130, 7, 2)])
+    (128, 64, 4), (64, 128, 3), (200, 136, 2), (37, 5, 2), (1, 40, 3), (130, 7, 2),
+    # tall, double-buffered kernel: ragged last row tile (partial 16-byte
+    # runs), several tiles per block of the resident grid
+    (1000, 132, 3), (520, 64, 5), (4096, 1536, 2), (130, 8, 2)])
 def test_apply_update(ns, h, rows, cols, count):
     rng = np.random.default_rng(7 * rows + cols)
     W = rng.standard_normal((count, rows, cols), dtype=np.float32)
