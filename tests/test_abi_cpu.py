@@ -126,3 +126,50 @@ def test_missing_library_fails_loudly(tmp_path):
                        text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.startswith("raised") and "is missing" in r.stdout
+
+
+def test_plan_invariants_on_random_group_lists(lib):
+    """Random group lists (shapes, counts, workspace caps, step counts): the
+    planner counts every matrix once, batches exactly the distinct wide
+    shapes, keeps chunks within the launch limits and the cap, and issues
+    per chunk one cast and one apply per caller segment, one norm and the
+    products."""
+    import numpy as np
+    rng = np.random.default_rng(2024)
+    dims = [1, 7, 64, 100, 128, 129, 256, 513, 1536, 2048, 4096]
+    for _ in range(300):
+        groups = []
+        for _ in range(int(rng.integers(1, 7))):
+            r, c = int(rng.choice(dims)), int(rng.choice(dims))
+            groups.append((r, c, int(rng.choice([0, 1, 2, 5, 40, 300]))))
+        steps = int(rng.choice([0, 1, 5, 7]))
+        cap = int(rng.choice([0, 1 << 20, 64 << 20, 1 << 30]))
+        info = lib.muon_plan_describe(groups, ns_steps=steps, workspace_bytes_max=cap)
+        live = [(min(r, c), max(r, c), k) for r, c, k in groups if k > 0]
+        shapes = {(m, n) for m, n, _ in live}
+        assert info["matrices"] == sum(k for _, _, k in live)
+        assert info["n_batches"] == len(shapes)
+        want = sum(k * o.ns_algorithmic_flops(m, n, steps) for m, n, k in live)
+        assert info["ns_algorithmic_flops"] == pytest.approx(want, rel=1e-12)
+        if not live:
+            assert info["n_chunks"] == 0 and info["launches_per_step"] == 0
+            continue
+        C, G, B = info["n_chunks"], len(live), len(shapes)
+        assert B <= C <= info["matrices"]
+        assert 1 <= info["max_chunk_matrices"] <= 65535
+        per_total = {}
+        for m, n, k in live:
+            per_total[(m, n)] = per_total.get((m, n), 0) + k
+        # No batch is cut into more chunks than its matrices need at the
+        # largest chunk size.
+        assert C >= sum(-(-t // info["max_chunk_matrices"]) for t in per_total.values())
+        products = 3 * steps if steps > 0 else 1
+        segs_lo, segs_hi = max(C, G), G + C - B
+        launches = info["launches_per_step"]
+        assert C * (1 + products) + 2 * segs_lo <= launches <= C * (1 + products) + 2 * segs_hi
+        # A cap that holds one matrix of each batch bounds the workspace
+        # (X twice, A and B, per-tile partials, padding and alignment).
+        one = max(4 * m * (n + 8) + 4 * m * (m + 8) + 4 * (-(-m // 64)) * (-(-n // 64)) + 4096
+                  for m, n in shapes)
+        if cap >= one:
+            assert info["workspace_bytes"] <= cap
