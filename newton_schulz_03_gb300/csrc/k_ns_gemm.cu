@@ -323,8 +323,9 @@ cudaError_t make_map(CUtensorMap* map, BatchView v, int cols, int rows, int coun
   return cudaSuccess;
 }
 
-// Output map for the TMA-store epilogue: 32 x 32 boxes, no swizzle (the
-// staging buffer is a dense 32 x 64-byte block).
+// Output map for the TMA-store epilogue: 32 x 32 boxes with the 64-byte
+// swizzle (the staging buffer holds the 32 rows x 64 bytes in that
+// pattern, so a quarter-warp's row writes hit distinct banks).
 cudaError_t make_map_out(CUtensorMap* map, BatchView v, int cols, int rows, int count) {
   EncodeFn enc = get_encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
