@@ -326,6 +326,19 @@ def run_ours(args, world, rank, local):
         "ns_engine_frac": round(ns_tflops / peak, 4) if ns_tflops else None,
         "kernel_time_share": kernel_share,
     }
+    # The HBM-bound kernels against the measured copy bandwidth: 14 B per
+    # element for the momentum update + cast (read M, G; write M, X) and
+    # 10 B for the apply (read W, O; write W).
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    elems_step = sum(g.count * g.rows * g.cols for g in w.groups) * layers
+    hbm_kernels = {}
+    for kind, bpe in (("momentum_cast", 14), ("apply", 10)):
+        ms = stats["total_ms"].get(kind, 0.0)
+        if ms > 0:
+            gbs = elems_step * bpe * steps_recorded / (ms / 1e3) / 1e9
+            hbm_kernels[kind] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                                 "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                                 "bytes_per_element": bpe}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -349,6 +362,7 @@ def run_ours(args, world, rank, local):
         "programmatic_dependent_launch": os.environ.get("MUON_PDL", "1") != "0",
         "clocks": clocks,
         "roofline": roofline,
+        "hbm_kernels": hbm_kernels,
     }
     if not args.skip_e2e:
         line["e2e"] = run_e2e(args, ns, h, w, groups, Ws, Ms, Gs, world)
