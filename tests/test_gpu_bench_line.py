@@ -1,0 +1,45 @@
+"""The benchmark's own arm on the GPU: one JSON line with the contract's
+keys (tiny workload, end-to-end leg and CPU baseline included)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_bench_json_line_contract():
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", "1", "--workload", "tiny",
+                        "--steps", "5", "--warmup", "3", "--cpu-seconds", "2"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
+        assert k in d, k
+    assert d["steps"] == 5 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["value"] > 0
+    assert d["config"]["workload"] == "tiny" and d["scaling"] == "weak"
+    # 18 library launches per step (cast, norm, 5 x 3 products, apply)
+    assert d["gpu_launches"] == 18 * 5
+    rf = d["roofline"]
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in rf, k
+    assert rf["bound"] == "tensor" and rf["achieved"] > 0 and rf["frac"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] > 0 and e["unit"] == d["unit"]
+    # tiny: 4 matrices of 128 x 64, M, G, W in (12 B/element), M, W out (8 B)
+    assert e["h2d_bytes_per_step"] == 4 * 128 * 64 * 12
+    assert e["d2h_bytes_per_step"] == 4 * 128 * 64 * 8
+    c = d["clocks"]
+    assert "sm_mhz" in c and "sm_max_mhz" in c and isinstance(c["reasons"], list)
