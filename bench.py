@@ -453,37 +453,60 @@ def cpu_cores() -> int:
     return os.cpu_count() or 1
 
 
-def oracle_sample_step(w, sample_matrices: int, seed_offset: int = 0):
-    """Run the oracle on `sample_matrices` matrices drawn from the workload's
-    groups (round robin over groups).  Returns (matrices, seconds)."""
+def oracle_shape_seconds(w, per_shape: int, seed_offset: int = 0):
+    """Time the oracle on `per_shape` matrices of every distinct wide shape
+    of the workload (a tall group costs what its wide transpose costs).
+    Returns ({wide shape: seconds per matrix}, matrices timed, seconds)."""
     import numpy as np
 
     from oracle import muon_oracle as o
     rng = np.random.default_rng(12345 + seed_offset)
-    done = 0
-    t0 = time.perf_counter()
-    gi = 0
-    while done < sample_matrices:
-        g = w.groups[gi % len(w.groups)]
-        gi += 1
-        W = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.w_std))
-        M = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.m_std))
-        G = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.g_std))
-        o.muon_step_matrix(W, M, G, lr=w.lr, wd=w.wd, mu=w.mu, ns_steps=w.ns_steps)
-        done += 1
-    return done, time.perf_counter() - t0
+    per, done, total = {}, 0, 0.0
+    for g in w.groups:
+        if g.wide in per:
+            continue
+        t0 = time.perf_counter()
+        for _ in range(per_shape):
+            W = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.w_std))
+            M = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.m_std))
+            G = (rng.standard_normal((g.rows, g.cols), dtype=np.float32) * np.float32(g.g_std))
+            o.muon_step_matrix(W, M, G, lr=w.lr, wd=w.wd, mu=w.mu, ns_steps=w.ns_steps)
+        dt = time.perf_counter() - t0
+        per[g.wide] = dt / per_shape
+        done += per_shape
+        total += dt
+    return per, done, total
+
+
+def workload_rate(w, per_matrix_seconds) -> float:
+    """Matrices per second over the whole workload, each group weighted by
+    its matrix count (exact for a single-shape workload)."""
+    secs = sum(g.count * per_matrix_seconds[g.wide] for g in w.groups)
+    return w.matrices_per_layer / secs
+
+
+def oracle_sample_text(w, per_shape: int, unit: str) -> str:
+    shapes = sorted({f"{m}x{n}" for m, n in w.wide_batches()})
+    text = (f"{per_shape} matrices {unit}of each wide shape ({', '.join(shapes)}) "
+            f"of workload {w.name}, FP64 NumPy oracle")
+    if len(shapes) > 1:
+        text += "; rate extrapolated over the workload's group counts"
+    return text
 
 
 def cpu_baseline(w, seconds_budget: float):
-    # Size the sample from one timed matrix so the leg takes ~seconds_budget.
-    n1, t1 = oracle_sample_step(w, 1, 0)
-    k = max(1, min(64, int(seconds_budget / max(t1, 1e-3)) - 1))
-    nk, tk = oracle_sample_step(w, k, 1)
-    n, t = n1 + nk, t1 + tk
-    shapes = sorted({f"{g.rows}x{g.cols}" for g in w.groups})
-    return {"value": round(n / t, 4), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{n} matrices ({', '.join(shapes)}) of workload {w.name}, FP64 NumPy "
-                      f"oracle, {t:.1f} s"}
+    # One matrix per shape first, then as many more as the budget allows.
+    per1, n1, t1 = oracle_shape_seconds(w, 1, 0)
+    k = int(seconds_budget / max(t1, 1e-3)) - 1
+    per, n, t = per1, n1, t1
+    if k >= 1:
+        k = min(64, k)
+        perk, nk, tk = oracle_shape_seconds(w, k, 1)
+        per = {s: (per1[s] + k * perk[s]) / (1 + k) for s in per1}
+        n, t = n1 + nk, t1 + tk
+    per_shape = n // len(per)
+    return {"value": round(workload_rate(w, per), 4), "unit": UNIT, "cores": cpu_cores(),
+            "kind": "oracle", "sample": oracle_sample_text(w, per_shape, "") + f", {t:.1f} s"}
 
 
 def run_reference(args, world, rank):
@@ -493,31 +516,30 @@ def run_reference(args, world, rank):
         return None
     w = WORKLOADS[args.workload]
     # Size one step to a bounded sample so the whole run takes minutes.
-    n1, t1 = oracle_sample_step(w, 1, 0)
+    _, _, t1 = oracle_shape_seconds(w, 1, 0)
     total_budget = 150.0
     if args.steps is None:
         args.steps = 10
     per_step = max(1, int(total_budget / (args.steps + args.warmup) / max(t1, 1e-3)))
-    per_step = min(per_step, w.matrices)
+    per_step = min(per_step, max(g.count for g in w.groups))
     for i in range(args.warmup):
-        oracle_sample_step(w, per_step, 100 + i)
-    done = 0
+        oracle_shape_seconds(w, per_step, 100 + i)
+    acc = {}
     secs = 0.0
     for i in range(args.steps):
-        n, t = oracle_sample_step(w, per_step, 1000 + i)
-        done += n
+        per, _, t = oracle_shape_seconds(w, per_step, 1000 + i)
+        for s_, v in per.items():
+            acc[s_] = acc.get(s_, 0.0) + v / args.steps
         secs += t
-    value = done / secs
-    shapes = sorted({f"{g.rows}x{g.cols}" for g in w.groups})
-    sample = (f"{per_step} matrices per step ({', '.join(shapes)}) of workload {w.name}, "
-              f"FP64 NumPy oracle")
+    value = workload_rate(w, acc)
+    sample = oracle_sample_text(w, per_step, "per step ")
     return {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs * 1e3 / args.steps, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": w.name, "matrices_per_step_sampled": per_step,
+        "config": {"workload": w.name, "matrices_per_step_sampled": per_step * len(acc),
                    "note": "CPU oracle on a bounded sample of the workload"},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},

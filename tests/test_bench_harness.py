@@ -99,3 +99,16 @@ def test_warmup_below_three_is_rejected():
                         "--steps", "1", "--warmup", "2"],
                        cwd=root, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_oracle_rate_weights_groups_by_count():
+    """A mixed workload's CPU rate weights each wide shape's time per matrix
+    by how many matrices of it the workload holds (tall groups count as
+    their wide transpose)."""
+    import bench
+    from newton_schulz_03_gb300.workloads import GroupSpec, Workload
+    w = Workload("mixed", "test", (GroupSpec("a", 64, 128, 6), GroupSpec("b", 256, 128, 1),
+                                   GroupSpec("c", 128, 256, 2)))
+    assert bench.workload_rate(w, {(64, 128): 1.0, (128, 256): 2.0}) == pytest.approx(9 / 12)
+    per, done, secs = bench.oracle_shape_seconds(w, 1)
+    assert set(per) == {(64, 128), (128, 256)} and done == 2 and secs > 0
