@@ -318,7 +318,8 @@ __device__ __forceinline__ void cp_async_wait_prior() {   // all groups but the 
 // with the next tile's O block prefetched into the other half of a double
 // buffer.  The 16-byte chunk q of buffer row j sits at chunk
 // q ^ ((j >> 2) & 7): the update reads one O element of each of 16 rows
-// j = 4k + e at a time, which without the swizzle share two banks.
+// j = 4k + e at a time; with 256-byte rows those would all fall in one
+// bank, with the swizzle they spread over eight (two-way at most).
 // Needs cols % 4 == 0, W 16-byte aligned, O pitches multiples of 8
 // elements and O 16-byte aligned.
 constexpr int kTallR = 128;   // W rows per tile (= O columns)
