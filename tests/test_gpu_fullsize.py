@@ -157,3 +157,45 @@ def test_fullsize_l102_layer(ns):
         check_sample(w, before, after, k)
     for k in heavy:
         check_heavy(w, before, after, k)
+
+
+def test_fullsize_l48_experts_variants(ns):
+    """The expert workload at full size through muon_step_ex with Nesterov
+    momentum, a per-iteration coefficient schedule and the RMS-matching
+    update scale, on sampled matrices of both orientations."""
+    from newton_schulz_03_gb300.workloads import WORKLOADS, make_group_torch
+    w = WORKLOADS["l48_experts"]
+    need = sum(g.numel for g in w.groups) * 12 + (9 << 30)
+    if free_bytes() < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free on the device")
+    sched = [(4.0848, -6.8946, 2.9270), (3.9505, -6.3029, 2.6377), (3.7418, -5.5913, 2.3037),
+             (2.8769, -3.1427, 1.2046), (2.8366, -3.0525, 1.2012)]
+    samples = [(0, 3), (1, 400)]
+    groups = [(g.rows, g.cols, g.count) for g in w.groups]
+    tensors = [make_group_torch(w, gi, "cuda") for gi in range(len(w.groups))]
+    before = {k: tuple(t[k[1]].cpu().numpy() for t in tensors[k[0]]) for k in samples}
+    Ws, Ms, Gs = ([t[k] for t in tensors] for k in range(3))
+    with ns.Handle() as h:
+        ns.muon_step_ex(h.value, groups, Ms, Gs, Ws, w.lr, w.wd, w.mu, 5, nesterov=True,
+                        coeffs=sched, scale_rule=ns.SCALE_RMS_MATCH)
+        ns.muon_last_device_error(h.value)
+    after = {k: (Ws[k[0]][k[1]].cpu().numpy(), Ms[k[0]][k[1]].cpu().numpy()) for k in samples}
+    del tensors, Ws, Ms, Gs
+    torch.cuda.empty_cache()
+    for (gi, i) in samples:
+        W, M, G = before[(gi, i)]
+        Wg, Mg = after[(gi, i)]
+        g = w.groups[gi]
+        scale = o.update_scale_rule(o.SCALE_RMS_MATCH, g.rows, g.cols)
+        kw = dict(lr=w.lr, wd=w.wd, mu=w.mu, ns_steps=5, coeffs=sched, nesterov=True,
+                  update_scale=scale)
+        st = o.muon_step_matrix(W, M, G, **kw)
+        assert ulp_close(Mg, st.M_new).all()
+        on = np.linalg.norm(st.O)
+        dw = np.linalg.norm(Wg.astype(np.float64) - st.W_new.astype(np.float64))
+        fp = 1e-6 * (np.linalg.norm(W) + w.lr * scale * on)
+        err = (dw - fp) / (w.lr * scale * on)
+        assert err <= NS_TOL, f"group {gi} matrix {i}: update error {err:.3e}"
+        emu = o.muon_step_matrix(W, M, G, emulate_bf16=True, **kw)
+        bound = 1.15 * np.linalg.norm(emu.O - st.O) / on + 5e-4
+        assert err <= bound, f"group {gi} matrix {i}: {err:.3e} vs error model {bound:.3e}"
