@@ -199,3 +199,25 @@ def test_fullsize_l48_experts_variants(ns):
         emu = o.muon_step_matrix(W, M, G, emulate_bf16=True, **kw)
         bound = 1.15 * np.linalg.norm(emu.O - st.O) / on + 5e-4
         assert err <= bound, f"group {gi} matrix {i}: {err:.3e} vs error model {bound:.3e}"
+
+
+def test_fullsize_l24_host_buffers_match_device_step(ns):
+    """The end-to-end entry point at the benchmark's size: muon_step_host on
+    pinned host buffers (pipelined pieces, ramped first and last pieces)
+    gives the device-buffer step's weights and momenta bit for bit."""
+    from newton_schulz_03_gb300.workloads import WORKLOADS, make_group_torch
+    w = WORKLOADS["l24_attention"]
+    need = sum(g.numel for g in w.groups) * 12 + (9 << 30)
+    if free_bytes() < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free on the device")
+    groups = [(g.rows, g.cols, g.count) for g in w.groups]
+    W, M, G = make_group_torch(w, 0, "cuda")
+    Wh, Mh, Gh = (t.cpu().pin_memory() for t in (W, M, G))
+    with ns.Handle() as h:
+        ns.muon_step_host(h.value, groups, [Mh], [Gh], [Wh], w.lr, w.wd, w.mu, w.ns_steps)
+        ns.muon_step(h.value, groups, [M], [G], [W], w.lr, w.wd, w.mu, w.ns_steps)
+        ns.muon_last_device_error(h.value)
+    assert torch.equal(Mh, M.cpu())
+    assert torch.equal(Wh, W.cpu())
+    del W, M, G
+    torch.cuda.empty_cache()
