@@ -75,9 +75,9 @@ typedef struct {
 typedef enum {
   MUON_KERNEL_MOMENTUM_CAST = 0,  /* momentum update + BF16 cast + transpose */
   MUON_KERNEL_NORM = 1,           /* per-matrix Frobenius norm finalisation */
-  MUON_KERNEL_NS_GRAM = 2,        /* A = alpha X X^T (upper tiles + mirror) */
-  MUON_KERNEL_NS_POLY = 3,        /* B = b A + c A A (upper tiles + mirror) */
-  MUON_KERNEL_NS_UPDATE = 4,      /* X' = alpha (a X + B X) */
+  MUON_KERNEL_NS_GRAM = 2,        /* A = alpha X X^T (symmetric storage, see below) */
+  MUON_KERNEL_NS_POLY = 3,        /* B' = a I + b A + c A A (same storage as A) */
+  MUON_KERNEL_NS_UPDATE = 4,      /* X' = alpha B' X  (= alpha (a X + b A X + c A^2 X)) */
   MUON_KERNEL_APPLY = 5,          /* W = W (1 - lr wd) - lr s O */
   MUON_KERNEL_SCALE = 6,          /* ns_steps == 0: O = X / s */
   MUON_KERNEL_ADAMW = 7,          /* AdamW companion */
@@ -135,6 +135,27 @@ muon_status_t muon_plan_describe(const muon_group_t* groups, int32_t n_groups,
                                  int32_t ns_steps, size_t workspace_bytes_max,
                                  muon_plan_info_t* out);
 
+/* Partition of a group list's whole matrices over `world` data-parallel
+ * ranks ("Scaling Muon to 16K GPUs", resharding step 2: after the
+ * exchange every GPU holds a subset of complete matrices and orthogonalises
+ * them independently, step 3).  Matrices are independent, so each rank
+ * steps its own subset with no exchange between ranks.
+ * The split is longest-processing-time-first over single matrices: in
+ * order of decreasing estimated device time (ns_steps*(3 m^2 n + m^3)
+ * algorithmic flops at 1.9 PFLOP/s plus 24 bytes per element at 6.8 TB/s),
+ * each matrix goes to the rank with the least estimated time so far.  A
+ * rank's matrices of one group are then laid out as one contiguous slice,
+ * ranks in order (same loads, since a group's matrices are identical).
+ * first_out, count_out: [n_groups * world] host arrays; entry g*world + r
+ *   receives the first matrix index and the matrix count of rank r's slice
+ *   of group g (count 0: none).  The slices of a group cover it exactly.
+ * rank_seconds_out: NULL or [world] host array: each rank's estimated time.
+ * Pure host computation, no GPU needed.  Errors: INVALID_ARG (bad groups,
+ * ns_steps outside 0..64, world outside 1..65536, NULL outputs). */
+muon_status_t muon_partition(const muon_group_t* groups, int32_t n_groups, int32_t ns_steps,
+                             int32_t world, int64_t* first_out, int32_t* count_out,
+                             double* rank_seconds_out);
+
 /* The whole Muon step on device buffers ("Scaling Muon to 16K GPUs",
  * resharding steps 1, 3, 5; "How to Make Parameter Updates Faster and More
  * Stable?").  For every matrix of every group:
@@ -166,6 +187,19 @@ muon_status_t muon_step_host(muon_handle_t handle, const muon_group_t* groups, i
                              float* const* momentum_host, const float* const* grad_host,
                              float* const* weights_host, float lr, float wd, float mu,
                              int32_t ns_steps, void* stream);
+
+/* Page-locked host memory for the buffers of muon_step_host
+ * (cudaHostAlloc, portable across devices).  Copies from it run at the
+ * host link's rate; on GB300 hosts measured here, memory locked after the
+ * fact with cudaHostRegister copied at a fraction of that rate once more
+ * than about 8 GiB of it was locked, while memory from this call kept the
+ * full rate.  *out receives the pointer (NULL on failure); free it with
+ * muon_host_free.  Errors: INVALID_ARG (out == NULL, bytes == 0), NOMEM. */
+muon_status_t muon_host_alloc(size_t bytes, void** out);
+
+/* Free memory from muon_host_alloc (NULL is accepted).  Synchronises with
+ * copies still reading or writing it.  Errors: CUDA. */
+muon_status_t muon_host_free(void* ptr);
 
 /* Shape rules for the update scale (common Muon variants; the pages give
  * no formula).  The factor multiplies each group's own update_scale. */
@@ -214,8 +248,18 @@ muon_status_t muon_momentum_cast(muon_handle_t handle, int32_t rows, int32_t col
 /* Step 3 alone: batched symmetric Newton-Schulz on `count` wide BF16
  * matrices m x n (m <= n), each pre-scaled by inv_norm[i]:
  *   X0 = inv_norm[i] * x[i]; ns_steps times X = a X + (b A + c A^2) X,
- *   A = X X^T.  Gram and square products compute only upper-triangle
- *   tiles and mirror them.
+ *   A = X X^T.
+ * Each iteration is three products, every result rounded to BF16 where
+ * it is stored:
+ *   Gram    A  = alpha X X^T            (alpha = inv_norm^2 at iteration 0, else 1)
+ *   square  B' = a I + b A + c A A      (the linear term folded into B')
+ *   update  X' = alpha B' X             (alpha = inv_norm at iteration 0, else 1)
+ * Storage of the symmetric A and B': for m > 128 only the 256 x 256 blocks
+ * on and above the block diagonal are computed and stored, nothing is
+ * mirrored, and a consumer reads a block left of the diagonal as the
+ * transpose of the stored block above it; for m <= 128 the matrix is one
+ * tile, computed once and stored in full (the part above the diagonal
+ * also written mirrored below it).
  * x_dev, out_dev: count*m*n BF16, 16-byte aligned, must not overlap.
  * inv_norm_dev:   count FP32 (device).
  * coeffs_host:    3 floats (a, b, c) or NULL for the defaults.
@@ -252,7 +296,9 @@ muon_status_t muon_apply_update(muon_handle_t handle, int32_t rows, int32_t cols
  *    (muon_last_error_message).  Larger counts are processed in passes.
  *  - First call on a device: resolves the array's device address
  *    (cudaGetSymbolAddress) and sets kernel attributes, with that device
- *    current.  Make that first call before any stream capture.
+ *    current.  Make that first call before any stream capture.  If that
+ *    set-up fails the call returns MUON_ERR_CUDA and the next call on the
+ *    device tries the set-up again.
  *  - Sharing: every call uses the same array and leaves its last contents
  *    there; nothing in it needs to start at zero (every scratch element is
  *    written before it is read).  Calls that overlap on the GPU (different

@@ -32,7 +32,7 @@ EXPORTED = (
     "muon_newton_schulz_bf16", "muon_apply_update", "muon_last_device_error",
     "muon_set_kernel_timing", "muon_kernel_stats", "muon_reset_kernel_stats",
     "muon_newton_schulz_bf16_static", "muon_selftest_bounded_wait", "muon_step_ex",
-    "muon_adamw_step",
+    "muon_adamw_step", "muon_partition", "muon_host_alloc", "muon_host_free",
 )
 SCALE_NONE, SCALE_SQRT_ASPECT, SCALE_RMS_MATCH = 0, 1, 2
 
@@ -96,6 +96,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "muon_create": (c_int, [P(c_vp), c_i32, c_sz]),
         "muon_destroy": (c_int, [c_vp]),
         "muon_plan_describe": (c_int, [P(_Group), c_i32, c_i32, c_sz, P(_PlanInfo)]),
+        "muon_host_alloc": (c_int, [c_sz, P(c_vp)]),
+        "muon_host_free": (c_int, [c_vp]),
+        "muon_partition": (c_int, [P(_Group), c_i32, c_i32, c_i32, P(ctypes.c_int64), P(c_i32),
+                                   P(ctypes.c_double)]),
         "muon_step": (c_int, [c_vp, P(_Group), c_i32, P(c_vp), P(c_vp), P(c_vp), c_f, c_f, c_f,
                               c_i32, c_vp]),
         "muon_step_host": (c_int, [c_vp, P(_Group), c_i32, P(c_vp), P(c_vp), P(c_vp), c_f, c_f,
@@ -209,6 +213,53 @@ def muon_plan_describe(groups: Sequence[GroupLike], ns_steps: int = 5,
     _check(load_library().muon_plan_describe(_groups(groups), len(groups), ns_steps,
                                              workspace_bytes_max, ctypes.byref(info)))
     return {f: getattr(info, f) for f, _ in _PlanInfo._fields_}
+
+
+def muon_host_alloc(nbytes: int) -> int:
+    """Page-locked host allocation (cudaHostAlloc); returns the address."""
+    p = ctypes.c_void_p()
+    _check(load_library().muon_host_alloc(nbytes, ctypes.byref(p)))
+    return p.value
+
+
+def muon_host_free(ptr: int) -> None:
+    _check(load_library().muon_host_free(ptr))
+
+
+def host_empty(shape, dtype=None):
+    """A CPU torch tensor (FP32 by default) in page-locked memory from
+    muon_host_alloc, freed when the tensor and its views are gone."""
+    import weakref
+
+    import numpy as np
+    import torch
+    dtype = dtype or torch.float32
+    n = 1
+    for d in shape:
+        n *= int(d)
+    itemsize = torch.empty((), dtype=dtype).element_size()
+    nbytes = max(1, n * itemsize)
+    ptr = muon_host_alloc(nbytes)
+    raw = (ctypes.c_uint8 * nbytes).from_address(ptr)
+    weakref.finalize(raw, muon_host_free, ptr)
+    arr = np.frombuffer(raw, dtype=np.uint8, count=n * itemsize)
+    return torch.from_numpy(arr).view(dtype).view(*shape)
+
+
+def muon_partition(groups: Sequence[GroupLike], world: int, ns_steps: int = 5):
+    """Whole-matrix split of a group list over `world` ranks.  Returns
+    (slices, seconds): slices[r] is a list of (group index, first, count)
+    of rank r's contiguous slices (count > 0 only); seconds[r] is rank r's
+    estimated device time."""
+    ng = len(groups)
+    first = (ctypes.c_int64 * max(1, ng * world))()
+    count = (ctypes.c_int32 * max(1, ng * world))()
+    secs = (ctypes.c_double * max(1, world))()
+    _check(load_library().muon_partition(_groups(groups), ng, ns_steps, world, first, count,
+                                         secs))
+    slices = [[(g, int(first[g * world + r]), int(count[g * world + r]))
+               for g in range(ng) if count[g * world + r] > 0] for r in range(world)]
+    return slices, [float(secs[r]) for r in range(world)]
 
 
 def muon_step(handle: int, groups: Sequence[GroupLike], momentum: Sequence, grad: Sequence,

@@ -11,6 +11,25 @@ namespace muon {
 constexpr int kDevErrTimeout = 1;
 constexpr int kDevErrNonFinite = 2;
 
+// Limits shared by every entry point: the longest matrix side, the
+// iteration count, and the largest grid.y of the elementwise kernels (one
+// grid row per matrix).
+constexpr int kMaxDim = 1 << 20;
+constexpr int kMaxSteps = 64;
+constexpr int64_t kMaxGridY = 65535;
+
+// Largest matrix count one Newton-Schulz launch sequence may cover: tile
+// indices stay in int32 (the update product has the most tiles,
+// ceil(m/128) * ceil(n/256); the Gram product t(t+1)/2 with t = ceil(m/128))
+// and the scale kernel of ns_steps == 0 keeps grid.y within its limit.
+inline int64_t ns_max_count_per_launch(int m, int n) {
+  const int64_t tm = (m + 127) / 128, tn = (n + 255) / 256;
+  const int64_t per = (tm * tn > tm * (tm + 1) / 2) ? tm * tn : tm * (tm + 1) / 2;
+  int64_t cap = (int64_t(1) << 30) / per;
+  if (cap > kMaxGridY) cap = kMaxGridY;
+  return cap < 1 ? 1 : cap;
+}
+
 // Elementwise kernels work on 64 x 64 tiles of the source matrix.
 constexpr int kEwTile = 64;
 
@@ -56,12 +75,13 @@ struct BatchView {
 cudaError_t ns_gemm_init();
 
 // A = alpha * X X^T, alpha = inv_norm[mat]^2 (or 1 when inv_norm == NULL).
-// X: m x n, A: m x m.  Upper-triangle tiles only, mirrored.
+// X: m x n, A: m x m.  m > 128: only the 256-blocks on and above the block
+// diagonal are computed and stored; m <= 128: one tile, stored in full.
 cudaError_t ns_launch_gram(int m, int n, int count, BatchView X, BatchView A_out,
                            const float* inv_norm, int* err, int grid_cap, cudaStream_t stream);
 
 // B' = a I + b A + c A A (A symmetric m x m): the quintic polynomial with
-// the linear term folded in.  Upper-triangle tiles only.
+// the linear term folded in.  Stored like A.
 cudaError_t ns_launch_poly(int m, int count, BatchView A, BatchView B_out, float a, float b,
                            float c, int* err, int grid_cap, cudaStream_t stream);
 

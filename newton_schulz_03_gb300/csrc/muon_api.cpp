@@ -47,18 +47,9 @@ muon_status_t cuda_fail(cudaError_t e, const char* what) {
 
 constexpr size_t kDefaultWorkspace = size_t(8) << 30;  // 8 GiB
 constexpr size_t kAlign = 256;
-constexpr int kMaxDim = 1 << 20;
-constexpr int kMaxSteps = 64;
+using muon::kMaxDim;
+using muon::kMaxSteps;
 constexpr int64_t kMaxMatrixElems = int64_t(1) << 34;
-
-// Largest matrix count per launch so that tile indices fit in int32 (the
-// update product has the most tiles: ceil(m/128) * ceil(n/256); the Gram
-// product has t(t+1)/2 with t = ceil(m/128)).
-int64_t max_count_per_launch(int m, int n) {
-  const int64_t tm = (m + 127) / 128, tn = (n + 255) / 256;
-  const int64_t per = std::max(tm * tn, tm * (tm + 1) / 2);
-  return std::max<int64_t>(1, (int64_t(1) << 30) / per);
-}
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
@@ -167,8 +158,7 @@ muon_status_t build_plan(const muon_group_t* groups, int32_t n_groups, int32_t n
     int64_t cap = static_cast<int64_t>((ws_cap > 8 * kAlign ? ws_cap - 8 * kAlign : 0) / pm);
     if (cap < 1) cap = 1;  // a single matrix always gets room
     if (cap > total) cap = total;
-    if (cap > 65535) cap = 65535;  // grid.y limit of the elementwise kernels
-    cap = std::min(cap, max_count_per_launch(m, n));
+    cap = std::min(cap, muon::ns_max_count_per_launch(m, n));  // also the grid.y limit
     P.ws_bytes = std::max(P.ws_bytes, chunk_layout(m, n, cap).bytes);
     P.matrices += total;
     P.flops += double(total) * ns_steps * (3.0 * m * double(m) * n + double(m) * m * m);
@@ -471,6 +461,65 @@ muon_status_t muon_plan_describe(const muon_group_t* groups, int32_t n_groups, i
   out->workspace_bytes = P.ws_bytes;
   out->ns_algorithmic_flops = P.flops;
   out->launches_per_step = P.launches;
+  return MUON_OK;
+}
+
+muon_status_t muon_partition(const muon_group_t* groups, int32_t n_groups, int32_t ns_steps,
+                             int32_t world, int64_t* first_out, int32_t* count_out,
+                             double* rank_seconds_out) {
+  muon_status_t st = validate_groups(groups, n_groups);
+  if (st != MUON_OK) return st;
+  if (ns_steps < 0 || ns_steps > kMaxSteps)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps out of range (%d)", ns_steps);
+  if (world < 1 || world > 65536) return fail(MUON_ERR_INVALID_ARG, "world out of range (%d)", world);
+  if (n_groups > 0 && (first_out == nullptr || count_out == nullptr))
+    return fail(MUON_ERR_INVALID_ARG, "first_out and count_out must not be NULL");
+  // Estimated device seconds of one matrix: its algorithmic Newton-Schulz
+  // flops at the tensor rate plus its elementwise bytes (momentum update +
+  // cast 14 B, apply 10 B per element) at the HBM rate.
+  constexpr double kFlopRate = 1.9e15, kByteRate = 6.8e12;
+  std::vector<double> cost(n_groups);
+  for (int g = 0; g < n_groups; ++g) {
+    const double m = std::min(groups[g].rows, groups[g].cols);
+    const double n = std::max(groups[g].rows, groups[g].cols);
+    cost[g] = ns_steps * (3.0 * m * m * n + m * m * m) / kFlopRate + 24.0 * m * n / kByteRate;
+  }
+  // Longest processing time first: matrices in order of decreasing cost
+  // (a group's matrices are identical, so a group is one run of the
+  // order), each to the rank with the least load so far.
+  std::vector<int> order(n_groups);
+  for (int g = 0; g < n_groups; ++g) order[g] = g;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  using Load = std::pair<double, int>;  // (seconds, rank): ties go to the lower rank
+  std::vector<Load> heap;
+  for (int r = 0; r < world; ++r) heap.push_back({0.0, r});
+  auto later = [](const Load& a, const Load& b) { return a > b; };
+  std::make_heap(heap.begin(), heap.end(), later);
+  std::vector<int64_t> per(size_t(n_groups) * world, 0);
+  for (int g : order) {
+    for (int64_t i = 0; i < groups[g].count; ++i) {
+      std::pop_heap(heap.begin(), heap.end(), later);
+      Load& least = heap.back();
+      least.first += cost[g];
+      per[size_t(g) * world + least.second] += 1;
+      std::push_heap(heap.begin(), heap.end(), later);
+    }
+  }
+  // A rank's matrices of one group form one contiguous slice (ranks in
+  // order), so each rank passes a group as one pointer and count.
+  std::vector<double> load(world, 0.0);
+  for (int g = 0; g < n_groups; ++g) {
+    int64_t first = 0;
+    for (int r = 0; r < world; ++r) {
+      const int64_t c = per[size_t(g) * world + r];
+      first_out[size_t(g) * world + r] = first;
+      count_out[size_t(g) * world + r] = static_cast<int32_t>(c);
+      load[r] += c * cost[g];
+      first += c;
+    }
+  }
+  if (rank_seconds_out != nullptr)
+    for (int r = 0; r < world; ++r) rank_seconds_out[r] = load[r];
   return MUON_OK;
 }
 
@@ -794,6 +843,27 @@ muon_status_t muon_step_host(muon_handle_t h, const muon_group_t* groups, int32_
   return MUON_OK;
 }
 
+muon_status_t muon_host_alloc(size_t bytes, void** out) {
+  if (out == nullptr) return fail(MUON_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (bytes == 0) return fail(MUON_ERR_INVALID_ARG, "bytes must be > 0");
+  cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *out = nullptr;
+    return fail(MUON_ERR_NOMEM, "page-locked host allocation of %zu bytes failed: %s", bytes,
+                cudaGetErrorString(e));
+  }
+  return MUON_OK;
+}
+
+muon_status_t muon_host_free(void* p) {
+  if (p == nullptr) return MUON_OK;
+  cudaError_t e = cudaFreeHost(p);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeHost");
+  return MUON_OK;
+}
+
 muon_status_t muon_momentum_cast(muon_handle_t h, int32_t rows, int32_t cols, int32_t count,
                                  float* momentum, const float* grad, float mu, uint16_t* x_wide,
                                  float* inv_norm, void* stream) {
@@ -864,7 +934,7 @@ muon_status_t muon_newton_schulz_bf16(muon_handle_t h, int32_t m, int32_t n, int
   int64_t cap = static_cast<int64_t>(h->ws_cap / pm);
   if (cap < 1) cap = 1;
   if (cap > count) cap = count;
-  cap = std::min(cap, max_count_per_launch(m, n));
+  cap = std::min(cap, muon::ns_max_count_per_launch(m, n));
   const size_t need = align_up(size_t(cap) * m * n * 2, kAlign) + 2 * align_up(size_t(cap) * m * m * 2, kAlign);
   st = ensure_workspace(h, need);
   if (st != MUON_OK) return st;

@@ -34,12 +34,15 @@ constexpr int kMaxDevices = 64;
 // device address comes from cudaGetSymbolAddress at set-up.
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
+// Per-device set-up state.  The address is latched only once a set-up
+// succeeded: a failed attempt (say, a first call made during a stream
+// capture) leaves `ready` unset and the next call tries again.
 struct DeviceSetup {
-  std::once_flag once;
-  cudaError_t status = cudaErrorNotReady;
+  bool ready = false;
   uint8_t* scratch = nullptr;  // device address of g_static_scratch
 };
 DeviceSetup g_setup[kMaxDevices];
+std::mutex g_setup_mutex;
 
 size_t align_s(size_t v) { return (v + kAlignS - 1) / kAlignS * kAlignS; }
 
@@ -51,16 +54,22 @@ muon_status_t fail_s(muon_status_t st, const char* msg) {
 // Once per device, with that device current: resolve the scratch address
 // and set the kernels' shared-memory attribute.
 cudaError_t setup_device(int dev, uint8_t** scratch) {
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
   DeviceSetup& S = g_setup[dev];
-  std::call_once(S.once, [&S]() {
+  if (!S.ready) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e == cudaSuccess) e = muon::ns_gemm_init();
-    if (e == cudaSuccess) S.scratch = static_cast<uint8_t*>(p);
-    S.status = e;
-  });
+    if (e != cudaSuccess) {
+      cudaGetLastError();  // leave no sticky-looking error behind; retry next call
+      *scratch = nullptr;
+      return e;
+    }
+    S.scratch = static_cast<uint8_t*>(p);
+    S.ready = true;
+  }
   *scratch = S.scratch;
-  return S.status;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -70,10 +79,11 @@ extern "C" muon_status_t muon_newton_schulz_bf16_static(int32_t m, int32_t n, in
                                                         const float* inv_norm_dev,
                                                         int32_t ns_steps, const float* coeffs_host,
                                                         int32_t* error_flag_dev, void* stream) {
-  if (m < 1 || n < 1 || m > n || count < 0 || (m % 8) != 0 || (n % 8) != 0)
+  if (m < 1 || n < 1 || m > n || m > muon::kMaxDim || n > muon::kMaxDim || count < 0 ||
+      (m % 8) != 0 || (n % 8) != 0)
     return fail_s(MUON_ERR_INVALID_ARG,
-                        "need 1 <= m <= n, both multiples of 8, and count >= 0");
-  if (ns_steps < 0 || ns_steps > 64)
+                  "need 1 <= m <= n <= 2^20, both multiples of 8, and count >= 0");
+  if (ns_steps < 0 || ns_steps > muon::kMaxSteps)
     return fail_s(MUON_ERR_INVALID_ARG, "ns_steps out of range");
   float a = MUON_NS_A, b = MUON_NS_B, c = MUON_NS_C;
   if (coeffs_host != nullptr) {
@@ -115,6 +125,7 @@ extern "C" muon_status_t muon_newton_schulz_bf16_static(int32_t m, int32_t n, in
   // Matrices per pass through the scratch; the batch is walked in passes.
   int64_t cap = static_cast<int64_t>((kStaticScratchBytes - kFlagBytes) / per);
   cap = std::min<int64_t>(cap, count);
+  cap = std::min<int64_t>(cap, muon::ns_max_count_per_launch(m, n));
   uint8_t* base = scratch + kFlagBytes;
   const size_t xs = align_s(size_t(cap) * m * n * 2), as = align_s(size_t(cap) * m * m * 2);
   uint16_t* other = reinterpret_cast<uint16_t*>(base);
