@@ -3,12 +3,16 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference]
 
-A step is one muon_step over one copy of the workload's parameter groups:
-momentum update + BF16 cast, Newton-Schulz on every matrix, weight update.
-Inputs are seeded synthetic tensors resident in HBM and larger than L2, so
-no flush is needed between steps.  With N > 1 (torchrun) every rank steps
-its own copy of the workload (independent matrices, no exchange), and the
-job value is all ranks' matrices over the slowest rank's time.
+A step is one muon_step over the workload's parameter groups: momentum
+update + BF16 cast, Newton-Schulz on every matrix, weight update.  The
+default workload is one full-scale layer of the largest model (L=102,
+hidden 8704: 1024 expert matrices of 2048 x 8704, the shared expert and
+four 8704 x 8704 attention projections; 226 GB of FP32 state).  Inputs are
+seeded synthetic tensors resident in HBM and larger than L2, so no flush is
+needed between steps.  With N > 1 (torchrun) the workload's whole matrices
+are split over the ranks by muon_partition (longest processing time
+first); every rank steps its own share with no exchange, and the job value
+is the workload's matrices over the slowest rank's time.
 
 The JSON line adds the roofline of the dominant kernel (the Newton-Schulz
 update product), measured live with CUDA events on the launching stream,
@@ -35,7 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = "NS-orthogonalised matrices/s and TFLOPS (% of GB300 BF16 peak); muon_step ms"
 UNIT = "matrices/s"
-DEFAULT_WORKLOAD = "l24_attention"
+DEFAULT_WORKLOAD = "l102_layer"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DOMINANT = "ns_update"
 NS_SOURCES = ("newton_schulz_03_gb300/csrc/k_ns_gemm.cu", "newton_schulz_03_gb300/csrc/k_ns_gemm2.cu",
@@ -60,10 +64,18 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def job_value(world: int, units_per_rank_step: float, steps: int, secs: float) -> float:
-    """Whole-job throughput: every rank processes its own units each step
-    (weak scaling); the job takes as long as the slowest rank."""
-    return world * units_per_rank_step * steps / secs
+def sig(x, digits: int = 6):
+    """`x` rounded to `digits` significant digits (None stays None)."""
+    if x is None:
+        return None
+    return float(f"{x:.{digits}g}")
+
+
+def job_value(units_per_step: float, steps: int, secs: float) -> float:
+    """Whole-job throughput: the ranks share one workload of
+    `units_per_step` matrices per step; the job takes as long as the
+    slowest rank."""
+    return units_per_step * steps / secs
 
 
 def barrier(world: int) -> None:
@@ -178,13 +190,15 @@ def ns_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, matrices_per_launch: float):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source.  The summary gives
-    bytes per matrix (traffic grows with the matrix count); one launch covers
-    ``matrices_per_launch`` matrices on average."""
+def profiled_traffic(workload: str, matrices_per_step: dict, launches_per_step: float):
+    """Average DRAM bytes per launch of the dominant kernel from the
+    committed ncu summary, if it was taken on the current kernel source.
+    The summary gives DRAM bytes per matrix for each wide shape
+    (``dram_bytes_per_matrix[MxN]``; traffic grows with the matrix count),
+    measured on a small case; one step's launches cover
+    ``matrices_per_step[(m, n)]`` matrices of each shape."""
     path = os.path.join(ROOT, "profiles", f"{DOMINANT}_{workload.split('[')[0]}.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or launches_per_step <= 0:
         return None
     kv = {}
     for line in open(path):
@@ -193,24 +207,59 @@ def profiled_traffic(workload: str, matrices_per_launch: float):
             kv[k.strip()] = v.strip()
     if kv.get("kernel_source_sha256_16") != ns_source_hash():
         return None
-    try:
-        return round(float(kv["dram_bytes_per_matrix"]) * matrices_per_launch)
-    except (KeyError, ValueError):
-        return None
+    total = 0.0
+    for (m, n), count in matrices_per_step.items():
+        key = f"dram_bytes_per_matrix[{m}x{n}]"
+        if key not in kv and len(matrices_per_step) == 1:
+            key = "dram_bytes_per_matrix"
+        try:
+            total += float(kv[key]) * count
+        except (KeyError, ValueError):
+            return None
+    return round(total / launches_per_step)
 
 
 # ----------------------------------------------------------------- our arm
-def capped(w, max_count):
-    """The workload with every group's count capped (small profiling cases)."""
-    if not max_count:
+def capped(w, max_count, shape=None):
+    """The workload with every group's count capped and, with `shape`
+    ("MxN"), only the groups of that wide shape (small profiling cases)."""
+    if not max_count and not shape:
         return w
     import dataclasses
-    gs = tuple(dataclasses.replace(g, count=min(g.count, max_count)) for g in w.groups)
-    return dataclasses.replace(w, name=f"{w.name}[count<={max_count}]", groups=gs)
+    gs = w.groups
+    name = w.name
+    if shape:
+        m, n = (int(v) for v in shape.lower().split("x"))
+        gs = tuple(g for g in gs if g.wide == (m, n))
+        if not gs:
+            raise SystemExit(f"workload {w.name} has no group of wide shape {shape}")
+        name += f"[{m}x{n}]"
+    if max_count:
+        gs = tuple(dataclasses.replace(g, count=min(g.count, max_count)) for g in gs)
+        name += f"[count<={max_count}]"
+    return dataclasses.replace(w, name=name, groups=gs)
 
 
 def workload_groups(w):
     return [(g.rows, g.cols, g.count) for g in w.groups]
+
+
+def rank_share(w, world, rank):
+    """This rank's slices of the workload: [(group index, first, count)]
+    from the library's whole-matrix partition (all of it at world = 1)."""
+    import newton_schulz_03_gb300 as ns
+    if world == 1:
+        return [(gi, 0, g.count) for gi, g in enumerate(w.groups) if g.count > 0]
+    slices, _ = ns.muon_partition(workload_groups(w), world, w.ns_steps)
+    return slices[rank]
+
+
+def share_wide_counts(w, share):
+    out = {}
+    for gi, _, count in share:
+        key = w.groups[gi].wide
+        out[key] = out.get(key, 0) + count
+    return out
 
 
 def run_ours(args, world, rank, local):
@@ -221,9 +270,10 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    w = capped(WORKLOADS[args.workload], args.max_count)
-    groups = workload_groups(w)
-    tensors = [make_group_torch(w, gi, dev) for gi in range(len(w.groups))]
+    w = capped(WORKLOADS[args.workload], args.max_count, args.shape)
+    share = rank_share(w, world, rank)
+    groups = [(w.groups[gi].rows, w.groups[gi].cols, count) for gi, _, count in share]
+    tensors = [make_group_torch(w, gi, dev, first, count) for gi, first, count in share]
     Ws = [t[0] for t in tensors]
     Ms = [t[1] for t in tensors]
     Gs = [t[2] for t in tensors]
@@ -231,11 +281,11 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream()
     handle = ns.Handle(device=local)
     h = handle.value
-    plan = ns.muon_plan_describe(groups, w.ns_steps)
+    plan_all = ns.muon_plan_describe(workload_groups(w), w.ns_steps)
     layers = w.layers
 
     def step_on(s):
-        # One step of the workload: `layers` calls over the resident layer.
+        # One step of this rank's share: `layers` calls over the resident layer.
         for _ in range(layers):
             ns.muon_step(h, groups, Ms, Gs, Ws, w.lr, w.wd, w.mu, w.ns_steps, s)
 
@@ -289,48 +339,57 @@ def run_ours(args, world, rank, local):
     gpu_launches = int(round((launches1 - launches0) * frac_timed))
 
     matrices_per_step = w.matrices
-    value = job_value(world, matrices_per_step, args.steps, secs)
+    value = job_value(matrices_per_step, args.steps, secs)
     ms_per_step = secs * 1e3 / args.steps
-    flops_step = plan["ns_algorithmic_flops"] * layers
-    tflops = world * flops_step * args.steps / secs / 1e12
+    flops_step = plan_all["ns_algorithmic_flops"] * layers
+    tflops = flops_step * args.steps / secs / 1e12
 
     peaks, peak_src = load_peaks()
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    # Dominant kernel: the update product X' = aX + BX, 2 m^2 n flops per matrix.
-    upd_flops_step = sum(c * 2.0 * mm * mm * nn for (mm, nn), c in w.wide_batches().items()) \
-        * w.ns_steps * layers
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # This rank's kernels: its own share of the workload.
+    mine = share_wide_counts(w, share)
+    my_flops_step = sum(c * w.ns_steps * (3.0 * m * m * n + m ** 3) for (m, n), c in mine.items()) \
+        * layers
+    # Dominant kernel: the update product X' = alpha B' X, 2 m^2 n flops per matrix.
+    upd_flops_step = sum(c * 2.0 * m * m * n for (m, n), c in mine.items()) * w.ns_steps * layers
     upd_launches = stats["launches"][DOMINANT]
     upd_ms = stats["total_ms"][DOMINANT]
     steps_recorded = args.steps + args.warmup
     achieved = (upd_flops_step * steps_recorded) / (upd_ms / 1e3) / 1e12 if upd_ms > 0 else None
     ns_ms = sum(stats["total_ms"][k] for k in ("ns_gram", "ns_poly", "ns_update"))
-    ns_tflops = (flops_step * steps_recorded) / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
+    ns_tflops = (my_flops_step * steps_recorded) / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
     kernel_share = {k: round(v / max(sum(stats["total_ms"].values()), 1e-9), 4)
                     for k, v in stats["total_ms"].items() if v > 0}
-    upd_matrices_step = sum(w.wide_batches().values()) * w.ns_steps * layers
-    traffic = profiled_traffic(w.name, upd_matrices_step * steps_recorded / upd_launches) \
+    upd_matrices_step = {k: c * w.ns_steps * layers for k, c in mine.items()}
+    traffic = profiled_traffic(w.name, upd_matrices_step, upd_launches / steps_recorded) \
         if upd_launches else None
     roofline = {
-        "kernel": ("ns_gemm_pair_kernel<update>" if min(m for m, _ in w.wide_batches()) > 128
+        "kernel": ("ns_gemm_pair_kernel<update>" if min(m for m, _ in mine) > 128
                    else "ns_gemm_kernel<update,256>") + " (X' = alpha B' X)",
-        "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
-        "peak": peak, "unit": "TFLOP/s",
-        "frac": round(achieved / peak, 4) if achieved else None,
-        "peak_source": f"{peak_src} bf16_tflops_sustained (of {peak_src})",
-        "frac_of_burst": round(achieved / burst, 4) if achieved else None,
+        "bound": "tensor", "achieved": sig(achieved),
+        "peak": burst, "unit": "TFLOP/s",
+        "frac": sig(achieved / burst) if achieved else None,
+        "peak_source": f"{peak_src} bf16_tflops, burst (of {peak_src})",
+        "peak_sustained": sustained,
+        "frac_of_sustained": sig(achieved / sustained) if achieved else None,
         "traffic": traffic,
+        "traffic_source": (f"profiles/{DOMINANT}_{w.name.split('[')[0]}.txt: ncu DRAM bytes per "
+                           "matrix on a small case x matrices per launch" if traffic else None),
         "launches": upd_launches,
-        "avg_launch_ms": round(upd_ms / upd_launches, 4) if upd_launches else None,
-        "ns_engine_tflops": round(ns_tflops, 1) if ns_tflops else None,
-        "ns_engine_frac": round(ns_tflops / peak, 4) if ns_tflops else None,
+        "avg_launch_ms": sig(upd_ms / upd_launches) if upd_launches else None,
+        "flops_per_launch": round(upd_flops_step * steps_recorded / upd_launches)
+        if upd_launches else None,
+        "ns_engine_tflops": sig(ns_tflops),
+        "ns_engine_frac": sig(ns_tflops / burst) if ns_tflops else None,
+        "ns_engine_frac_of_sustained": sig(ns_tflops / sustained) if ns_tflops else None,
         "kernel_time_share": kernel_share,
     }
     # The HBM-bound kernels against the measured copy bandwidth: 14 B per
     # element for the momentum update + cast (read M, G; write M, X) and
     # 10 B for the apply (read W, O; write W).
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    elems_step = sum(g.count * g.rows * g.cols for g in w.groups) * layers
+    elems_step = sum(w.groups[gi].rows * w.groups[gi].cols * c for gi, _, c in share) * layers
     hbm_kernels = {}
     for kind, bpe in (("momentum_cast", 14), ("apply", 10)):
         ms = stats["total_ms"].get(kind, 0.0)
@@ -342,19 +401,21 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded torch RNG on device, shapes of the workload)",
         "config": {
             "workload": w.name, "description": w.description,
-            "matrices_per_step": matrices_per_step, "groups": groups, "layers": layers,
-            "ns_steps": w.ns_steps, "mu": w.mu, "lr": w.lr, "wd": w.wd,
+            "matrices_per_step": matrices_per_step, "groups": workload_groups(w),
+            "layers": layers, "ns_steps": w.ns_steps, "mu": w.mu, "lr": w.lr, "wd": w.wd,
             "precision": "FP32 momentum and weights, BF16 Newton-Schulz with FP32 accumulation",
             "l2": "inputs larger than L2 (%.1f GB of FP32 state per layer), no flush"
                   % (sum(g.numel for g in w.groups) * 12 / 1e9),
-            "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
+            "parallelism": (f"{world} ranks, whole matrices split by muon_partition (LPT), "
+                            "no exchange" if world > 1 else "single GPU"),
         },
         "tflops_algorithmic": round(tflops, 1),
-        "pct_of_bf16_peak": round(100 * tflops / peak, 2),
+        "pct_of_bf16_peak": round(100 * tflops / burst, 2),
+        "pct_of_bf16_sustained": round(100 * tflops / sustained, 2),
         "tflops_dense_equivalent": round(tflops * dense_over_alg(w), 1),
         "gpu_launches": gpu_launches,
         "graph_replay_ms_per_step": round(graph_ms, 4) if graph_ms is not None else None,
@@ -365,7 +426,7 @@ def run_ours(args, world, rank, local):
         "hbm_kernels": hbm_kernels,
     }
     if not args.skip_e2e:
-        line["e2e"] = run_e2e(args, ns, h, w, groups, Ws, Ms, Gs, world)
+        line["e2e"] = run_e2e(args, ns, h, w, share, Ws, Ms, Gs, world)
     if args.adamw:
         line["adamw"] = run_adamw(ns, h, peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -415,34 +476,100 @@ def dense_over_alg(w) -> float:
     return dense / alg
 
 
-def run_e2e(args, ns, h, w, groups, Ws, Ms, Gs, world):
-    """The same step through muon_step_host: pinned host buffers, H2D of
-    momentum, gradient and weights and D2H of momentum and weights inside
-    the timed region."""
+def host_available_bytes() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def e2e_passes(group_counts, elems_per_matrix, budget_bytes) -> int:
+    """Smallest power of two P such that host buffers holding 1/P of every
+    group whose count P divides (and the other groups whole) fit the budget
+    (12 bytes per element: momentum, gradient, weights)."""
+    p = 1
+    while True:
+        held = sum((c // p if c % p == 0 else c) * e * 12
+                   for c, e in zip(group_counts, elems_per_matrix))
+        if held <= budget_bytes or p >= max(group_counts + [1]):
+            return p
+        p *= 2
+
+
+# Pinned host footprint of the end-to-end leg.  On the GB300 hosts measured
+# here, copies from cudaHostAlloc memory ran at the link's ~210 GB/s up to
+# 16-32 GiB of it and slowed beyond; 20 GiB keeps the leg link-bound.
+E2E_HOST_BYTES = 20 << 30
+
+
+def run_e2e(args, ns, h, w, share, Ws, Ms, Gs, world):
+    """The same step through muon_step_host: page-locked host buffers
+    (muon_host_alloc), H2D of momentum, gradient and weights and D2H of
+    momentum and weights inside the timed region.
+
+    When the rank's whole share does not fit the pinned host budget (the
+    L=102 layer is 226 GB of FP32 state), the host buffers hold 1/P of
+    every group whose count P divides (the routed experts) and the others
+    whole, and one step is P calls: the first over every group, the other
+    P-1 over the divided groups again.  Each step then copies and steps as
+    many matrices of each shape as the device step (the same bytes and
+    flops); the values of the divided groups repeat."""
     import torch
-    hW = [t.cpu().pin_memory() for t in Ws]
-    hM = [t.cpu().pin_memory() for t in Ms]
-    hG = [t.cpu().pin_memory() for t in Gs]
+    counts = [c for _, _, c in share]
+    elems = [w.groups[gi].rows * w.groups[gi].cols for gi, _, _ in share]
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    avail = host_available_bytes() // (2 * max(1, local_ranks))
+    budget = min(E2E_HOST_BYTES, avail) if avail > 0 else E2E_HOST_BYTES
+    P = e2e_passes(counts, elems, budget)
+    held = [c // P if (P > 1 and c % P == 0) else c for c in counts]
+    divided = [P > 1 and c % P == 0 for c in counts]
+    host = []
+    for i, (gi, _, _) in enumerate(share):
+        g = w.groups[gi]
+        trip = []
+        for dev_t in (Ws[i], Ms[i], Gs[i]):
+            t = ns.host_empty((held[i], g.rows, g.cols))
+            t.copy_(dev_t[:held[i]])
+            trip.append(t)
+        host.append(trip)
+    torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
+    gs_all = [(w.groups[gi].rows, w.groups[gi].cols, held[i]) for i, (gi, _, _) in enumerate(share)]
+    div_idx = [i for i in range(len(share)) if divided[i]]
 
     def step():
         for _ in range(w.layers):
-            ns.muon_step_host(h, groups, hM, hG, hW, w.lr, w.wd, w.mu, w.ns_steps, stream)
+            ns.muon_step_host(h, gs_all, [t[1] for t in host], [t[2] for t in host],
+                              [t[0] for t in host], w.lr, w.wd, w.mu, w.ns_steps, stream)
+            for _ in range(P - 1):
+                ns.muon_step_host(h, [gs_all[i] for i in div_idx], [host[i][1] for i in div_idx],
+                                  [host[i][2] for i in div_idx], [host[i][0] for i in div_idx],
+                                  w.lr, w.wd, w.mu, w.ns_steps, stream)
 
     steps = max(1, min(args.steps, args.e2e_steps))
-    for _ in range(1):
-        step()
+    step()
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(steps):
         step()
     secs = max_over_ranks(time.perf_counter() - t0, world,
                           device=torch.device("cuda", torch.cuda.current_device()))
-    nbytes = sum(g.numel for g in w.groups) * 4 * w.layers
-    return {"value": round(world * w.matrices * steps / secs, 3), "unit": UNIT,
+    nbytes = sum(c * e for c, e in zip(counts, elems)) * 4 * w.layers
+    held_gb = sum(hc * e for hc, e in zip(held, elems)) * 12 / 1e9
+    del host
+    api = "muon_step_host (page-locked host buffers from muon_host_alloc)"
+    if P > 1:
+        api += (f"; host buffers hold 1/{P} of every group whose count {P} divides "
+                f"({held_gb:.1f} GB pinned) and one step is {P} calls, so every step copies "
+                "and steps the whole workload")
+    return {"value": round(w.matrices * steps / secs, 3), "unit": UNIT,
             "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
-            "steps": steps, "ms_per_step": round(secs * 1e3 / steps, 3),
-            "api": "muon_step_host (pinned host buffers)"}
+            "steps": steps, "ms_per_step": round(secs * 1e3 / steps, 3), "api": api,
+            "host_passes": P, "host_pinned_gb": round(held_gb, 2)}
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -453,17 +580,24 @@ def cpu_cores() -> int:
     return os.cpu_count() or 1
 
 
-def oracle_shape_seconds(w, per_shape: int, seed_offset: int = 0):
+def oracle_flops(m: int, n: int, steps: int) -> float:
+    """Flops of the oracle's plain iteration on an m x n wide matrix (no
+    symmetry: X X^T, A A and B X, 2 m^2 n + 2 m^3 + 2 m^2 n per step)."""
+    return steps * (4.0 * m * m * n + 2.0 * m ** 3)
+
+
+def oracle_shape_seconds(w, per_shape: int, seed_offset: int = 0, shapes=None):
     """Time the oracle on `per_shape` matrices of every distinct wide shape
-    of the workload (a tall group costs what its wide transpose costs).
-    Returns ({wide shape: seconds per matrix}, matrices timed, seconds)."""
+    of the workload (or of `shapes` only; a tall group costs what its wide
+    transpose costs).  Returns ({wide shape: seconds per matrix}, matrices
+    timed, seconds)."""
     import numpy as np
 
     from oracle import muon_oracle as o
     rng = np.random.default_rng(12345 + seed_offset)
     per, done, total = {}, 0, 0.0
     for g in w.groups:
-        if g.wide in per:
+        if g.wide in per or (shapes is not None and g.wide not in shapes):
             continue
         t0 = time.perf_counter()
         for _ in range(per_shape):
@@ -478,6 +612,34 @@ def oracle_shape_seconds(w, per_shape: int, seed_offset: int = 0):
     return per, done, total
 
 
+def split_shapes(w, budget: float):
+    """Wide shapes the oracle times (one matrix costs at most budget/3 at
+    the FP64 rate of one matrix of the cheapest shape) and shapes whose
+    time per matrix is extrapolated from the measured rate by their oracle
+    flop count.  Returns (timed, extrapolated, probe seconds per matrix)."""
+    shapes = sorted(w.wide_batches(), key=lambda s: oracle_flops(s[0], s[1], w.ns_steps))
+    cheapest = shapes[0]
+    per, _, _ = oracle_shape_seconds(w, 1, 7, shapes={cheapest})
+    rate = oracle_flops(*cheapest, w.ns_steps) / max(per[cheapest], 1e-9)
+    timed = [s for s in shapes if oracle_flops(*s, w.ns_steps) / rate <= budget / 3.0]
+    if cheapest not in timed:
+        timed.insert(0, cheapest)
+    extra = [s for s in shapes if s not in timed]
+    return timed, extra, per[cheapest]
+
+
+def complete_per_matrix(w, per, extra):
+    """Fill in the extrapolated shapes at the FP64 rate the timed shapes
+    reached (their flops over their seconds)."""
+    fl = sum(oracle_flops(m, n, w.ns_steps) for m, n in per)
+    secs = sum(per.values())
+    rate = fl / max(secs, 1e-12)
+    out = dict(per)
+    for m, n in extra:
+        out[(m, n)] = oracle_flops(m, n, w.ns_steps) / rate
+    return out
+
+
 def workload_rate(w, per_matrix_seconds) -> float:
     """Matrices per second over the whole workload, each group weighted by
     its matrix count (exact for a single-shape workload)."""
@@ -485,28 +647,31 @@ def workload_rate(w, per_matrix_seconds) -> float:
     return w.matrices_per_layer / secs
 
 
-def oracle_sample_text(w, per_shape: int, unit: str) -> str:
-    shapes = sorted({f"{m}x{n}" for m, n in w.wide_batches()})
-    text = (f"{per_shape} matrices {unit}of each wide shape ({', '.join(shapes)}) "
+def oracle_sample_text(w, per_shape: int, unit: str, timed, extra) -> str:
+    fmt = lambda ss: ", ".join(f"{m}x{n}" for m, n in ss)  # noqa: E731
+    text = (f"{per_shape} matrices {unit}of each timed wide shape ({fmt(timed)}) "
             f"of workload {w.name}, FP64 NumPy oracle")
-    if len(shapes) > 1:
+    if extra:
+        text += (f"; {fmt(extra)} not timed (one matrix is too long for the sample): time per "
+                 "matrix extrapolated from the timed shapes' FP64 rate by the oracle's flop "
+                 "count ns_steps*(4 m^2 n + 2 m^3)")
+    if len(timed) + len(extra) > 1:
         text += "; rate extrapolated over the workload's group counts"
     return text
 
 
 def cpu_baseline(w, seconds_budget: float):
-    # One matrix per shape first, then as many more as the budget allows.
-    per1, n1, t1 = oracle_shape_seconds(w, 1, 0)
-    k = int(seconds_budget / max(t1, 1e-3)) - 1
-    per, n, t = per1, n1, t1
-    if k >= 1:
-        k = min(64, k)
-        perk, nk, tk = oracle_shape_seconds(w, k, 1)
-        per = {s: (per1[s] + k * perk[s]) / (1 + k) for s in per1}
-        n, t = n1 + nk, t1 + tk
-    per_shape = n // len(per)
-    return {"value": round(workload_rate(w, per), 4), "unit": UNIT, "cores": cpu_cores(),
-            "kind": "oracle", "sample": oracle_sample_text(w, per_shape, "") + f", {t:.1f} s"}
+    t0 = time.perf_counter()
+    timed, extra, probe = split_shapes(w, seconds_budget)
+    one = sum(oracle_flops(m, n, w.ns_steps) for m, n in timed) / \
+        oracle_flops(*timed[0], w.ns_steps) * probe
+    k = int(max(1, min(64, seconds_budget / max(one, 1e-3))))
+    per, n, _ = oracle_shape_seconds(w, k, 1, shapes=set(timed))
+    full = complete_per_matrix(w, per, extra)
+    t = time.perf_counter() - t0
+    return {"value": round(workload_rate(w, full), 4), "unit": UNIT, "cores": cpu_cores(),
+            "kind": "oracle",
+            "sample": oracle_sample_text(w, k, "", timed, extra) + f", {t:.1f} s"}
 
 
 def run_reference(args, world, rank):
@@ -515,29 +680,32 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     w = WORKLOADS[args.workload]
-    # Size one step to a bounded sample so the whole run takes minutes.
-    _, _, t1 = oracle_shape_seconds(w, 1, 0)
-    total_budget = 150.0
     if args.steps is None:
         args.steps = 10
-    per_step = max(1, int(total_budget / (args.steps + args.warmup) / max(t1, 1e-3)))
+    # Size one step to a bounded sample so the whole run takes minutes.
+    total_budget = 150.0
+    per_step_budget = total_budget / (args.steps + args.warmup)
+    timed, extra, probe = split_shapes(w, max(per_step_budget, 3.0))
+    one = sum(oracle_flops(m, n, w.ns_steps) for m, n in timed) / \
+        oracle_flops(*timed[0], w.ns_steps) * probe
+    per_step = max(1, int(per_step_budget / max(one, 1e-3)))
     per_step = min(per_step, max(g.count for g in w.groups))
     for i in range(args.warmup):
-        oracle_shape_seconds(w, per_step, 100 + i)
+        oracle_shape_seconds(w, per_step, 100 + i, shapes=set(timed))
     acc = {}
     secs = 0.0
     for i in range(args.steps):
-        per, _, t = oracle_shape_seconds(w, per_step, 1000 + i)
+        per, _, t = oracle_shape_seconds(w, per_step, 1000 + i, shapes=set(timed))
         for s_, v in per.items():
             acc[s_] = acc.get(s_, 0.0) + v / args.steps
         secs += t
-    value = workload_rate(w, acc)
-    sample = oracle_sample_text(w, per_step, "per step ")
+    value = workload_rate(w, complete_per_matrix(w, acc, extra))
+    sample = oracle_sample_text(w, per_step, "per step ", timed, extra)
     return {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs * 1e3 / args.steps, 2), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "scaling": "strong", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
         "config": {"workload": w.name, "matrices_per_step_sampled": per_step * len(acc),
                    "note": "CPU oracle on a bounded sample of the workload"},
@@ -560,6 +728,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--max-count", type=int, default=0,
                     help="cap every group's matrix count (small profiling cases)")
+    ap.add_argument("--shape", default=None,
+                    help="keep only the groups of this wide shape, e.g. 2048x8704 (profiling)")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured in a CUDA graph and replayed")

@@ -145,25 +145,36 @@ def make_group_numpy(workload: Workload, group_index: int):
     return W, M, G
 
 
-def make_group_torch(workload: Workload, group_index: int, device: str = "cuda"):
-    """(W, M, G) as FP32 torch tensors [count, rows, cols], drawn on
-    ``device`` by torch's seeded generator (used where the host cannot hold
-    a whole workload)."""
+def make_group_torch(workload: Workload, group_index: int, device: str = "cuda",
+                     first: int = 0, count: Optional[int] = None):
+    """(W, M, G) as FP32 torch tensors [count, rows, cols] for matrices
+    first .. first+count-1 of a group (default: the whole group), drawn on
+    ``device`` (used where the host cannot hold a whole workload).  Matrix
+    i is drawn by its own seeded generator, so a slice of a group has the
+    same values whether it is made alone (one rank's share) or as part of
+    the whole group."""
     import torch
     g = workload.groups[group_index]
+    if count is None:
+        count = g.count - first
+    shape = (count, g.rows, g.cols)
+    W = torch.empty(shape, device=device, dtype=torch.float32)
+    M = torch.empty(shape, device=device, dtype=torch.float32)
+    G = torch.empty(shape, device=device, dtype=torch.float32)
     gen = torch.Generator(device=device)
-    gen.manual_seed(group_seed(workload, group_index))
-    shape = (g.count, g.rows, g.cols)
-    W = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).mul_(g.w_std)
-    M = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).mul_(g.m_std)
-    G = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).mul_(g.g_std)
+    for j in range(count):
+        gen.manual_seed((group_seed(workload, group_index) << 20) + first + j)
+        W[j].normal_(0.0, g.w_std, generator=gen)
+        M[j].normal_(0.0, g.m_std, generator=gen)
+        G[j].normal_(0.0, g.g_std, generator=gen)
     if g.expert_scaled:
-        sc = torch.from_numpy(np.exp(expert_log_scales(workload, g.count)).astype(np.float32)).to(device)
+        sc = np.exp(expert_log_scales(workload, g.count)[first:first + count]).astype(np.float32)
+        sc = torch.from_numpy(sc).to(device)
         M.mul_(sc[:, None, None])
         G.mul_(sc[:, None, None])
-    if g.zero_index is not None and g.zero_index < g.count:
-        M[g.zero_index].zero_()
-        G[g.zero_index].zero_()
+    if g.zero_index is not None and first <= g.zero_index < first + count:
+        M[g.zero_index - first].zero_()
+        G[g.zero_index - first].zero_()
     return W, M, G
 
 

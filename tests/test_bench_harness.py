@@ -1,5 +1,6 @@
 """The benchmark's multi-rank harness on CPU (gloo, world size 2): barrier,
-max-over-ranks timing and the weak-scaling job value."""
+max-over-ranks timing, the job value over the slowest rank, the ranks' shares
+of the workload, the end-to-end host passes and the CPU baseline's sample."""
 
 import os
 import socket
@@ -43,12 +44,63 @@ def test_max_over_ranks_gloo():
     assert dict(out) == {0: 2.0, 1: 2.0}
 
 
-def test_job_value_weak_scaling():
+def test_job_value_over_the_slowest_rank():
+    """The ranks share one workload: the job value is the workload's
+    matrices per step over the slowest rank's time, whatever the rank count."""
     import bench
-    one = bench.job_value(1, 96, 20, 0.3)
-    two = bench.job_value(2, 96, 20, 0.3)
-    assert two == pytest.approx(2 * one)
-    assert bench.job_value(4, 96, 20, 0.6) == pytest.approx(2 * one)
+    assert bench.job_value(1030, 20, 10.0) == pytest.approx(2060.0)
+    assert bench.job_value(1030, 20, 5.0) == pytest.approx(2 * bench.job_value(1030, 20, 10.0))
+
+
+def test_e2e_host_passes_fit_the_budget():
+    """The end-to-end leg holds 1/P of every group whose count P divides:
+    the L=102 layer (226 GB of FP32 state) needs P = 4 under a 98 GB host
+    budget (58 GB held) and P = 16 under the leg's 20 GiB pinned budget
+    (13.7 GB of experts + the 6.3 GB shared expert and attention held
+    whole); a workload that fits is held whole."""
+    import bench
+    from newton_schulz_03_gb300.workloads import WORKLOADS
+    w = WORKLOADS["l102_layer"]
+    counts = [g.count for g in w.groups]
+    elems = [g.rows * g.cols for g in w.groups]
+    assert bench.e2e_passes(counts, elems, 98 << 30) == 4
+    assert bench.e2e_passes(counts, elems, bench.E2E_HOST_BYTES) == 16
+    assert bench.e2e_passes(counts, elems, 300 << 30) == 1
+    w24 = WORKLOADS["l24_attention"]
+    assert bench.e2e_passes([96], [2048 * 2048], 98 << 30) == 1
+    assert bench.e2e_passes([w24.groups[0].count], [2048 * 2048], 1 << 30) == 8
+
+
+def test_rank_shares_partition_the_workload():
+    """bench.py's ranks step disjoint slices that cover the workload."""
+    import bench
+    from newton_schulz_03_gb300.workloads import WORKLOADS
+    w = WORKLOADS["l102_layer"]
+    for world in (1, 2, 4, 8):
+        seen = {}
+        for rank in range(world):
+            for gi, first, count in bench.rank_share(w, world, rank):
+                seen.setdefault(gi, []).append((first, count))
+        for gi, g in enumerate(w.groups):
+            spans = sorted(seen[gi])
+            assert spans[0][0] == 0 and sum(c for _, c in spans) == g.count
+            assert all(a + c == b for (a, c), (b, _) in zip(spans, spans[1:]))
+
+
+def test_cpu_baseline_extrapolates_shapes_too_long_for_the_sample():
+    """On the L=102 layer the oracle times the 2048 x 8704 experts and
+    extrapolates 8704 x 8704 and 8704 x 13056 (tens of seconds each) by
+    their flop count at the measured FP64 rate."""
+    import bench
+    from newton_schulz_03_gb300.workloads import WORKLOADS
+    w = WORKLOADS["l102_layer"]
+    per = {(2048, 8704): 2.0}
+    full = bench.complete_per_matrix(w, per, [(8704, 8704), (8704, 13056)])
+    f = bench.oracle_flops
+    assert full[(8704, 8704)] == pytest.approx(2.0 * f(8704, 8704, 5) / f(2048, 8704, 5))
+    assert full[(8704, 13056)] == pytest.approx(2.0 * f(8704, 13056, 5) / f(2048, 8704, 5))
+    text = bench.oracle_sample_text(w, 3, "", [(2048, 8704)], [(8704, 8704), (8704, 13056)])
+    assert "extrapolated" in text and "8704x13056" in text
 
 
 def test_reference_arm_other_ranks_exit_quietly():

@@ -27,13 +27,19 @@ def test_bench_json_line_contract():
               "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
         assert k in d, k
     assert d["steps"] == 5 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["value"] > 0
-    assert d["config"]["workload"] == "tiny" and d["scaling"] == "weak"
+    assert d["config"]["workload"] == "tiny" and d["scaling"] == "strong"
     # 18 library launches per step (cast, norm, 5 x 3 products, apply)
     assert d["gpu_launches"] == 18 * 5
     rf = d["roofline"]
     for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert k in rf, k
     assert rf["bound"] == "tensor" and rf["achieved"] > 0 and rf["frac"] > 0
+    # frac is against the measured burst peak; the sustained one is beside it
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], rel=1e-3)
+    assert rf["frac_of_sustained"] == pytest.approx(rf["achieved"] / rf["peak_sustained"],
+                                                    rel=1e-3)
+    assert rf["achieved"] == pytest.approx(rf["flops_per_launch"] / (rf["avg_launch_ms"] * 1e9),
+                                           rel=1e-4)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
     e = d["e2e"]
