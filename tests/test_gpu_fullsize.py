@@ -2,11 +2,10 @@
 configuration the benchmark times (one muon_step over every group of the
 workload), checked on sampled matrices against the CPU oracle.
 
-Matrices the FP64 oracle cannot finish in seconds (8704 x 8704 and
-8704 x 13056) are checked through properties that hold at any size: the
-momentum update and cast element-wise, and for the orthogonalised update
-the symmetry of O X0^T (= q(A) A for the polynomial q of the iteration)
-plus agreement with an FP32 re-statement of the iteration on cuBLAS.
+Every configured shape meets the FP64 oracle here, the largest ones
+included: an 8704 x 8704 attention projection and the 8704 x 13056 shared
+expert of the L=102 layer take the oracle about a minute each on the host
+cores.
 """
 
 import numpy as np
@@ -35,7 +34,7 @@ def free_bytes():
     return free
 
 
-def step_workload(ns, wname, samples, heavy=None):
+def step_workload(ns, wname, samples):
     """Step a whole workload once on device-generated inputs; return the
     sampled matrices' inputs and outputs on the host."""
     from newton_schulz_03_gb300.workloads import WORKLOADS, make_group_torch
@@ -46,13 +45,13 @@ def step_workload(ns, wname, samples, heavy=None):
     groups = [(g.rows, g.cols, g.count) for g in w.groups]
     tensors = [make_group_torch(w, gi, "cuda") for gi in range(len(w.groups))]
     before = {(gi, i): tuple(t[i].cpu().numpy() for t in tensors[gi])
-              for gi, i in samples + (heavy or [])}
+              for gi, i in samples}
     Ws, Ms, Gs = ([t[k] for t in tensors] for k in range(3))
     with ns.Handle() as h:
         ns.muon_step(h.value, groups, Ms, Gs, Ws, w.lr, w.wd, w.mu, w.ns_steps)
         ns.muon_last_device_error(h.value)
     after = {(gi, i): (Ws[gi][i].cpu().numpy(), Ms[gi][i].cpu().numpy())
-             for gi, i in samples + (heavy or [])}
+             for gi, i in samples}
     del tensors, Ws, Ms, Gs
     torch.cuda.empty_cache()
     return w, before, after
@@ -83,47 +82,8 @@ def check_sample(w, before, after, key, model=False):
     return err
 
 
-def check_heavy(w, before, after, key):
-    """Property checks for a matrix too large for the FP64 oracle."""
-    gi, i = key
-    W, M, G = before[key]
-    Wg, Mg = after[key]
-    Mref = o.momentum_update(M, G, w.mu)
-    assert ulp_close(Mg, Mref).all()
-    # Recover the GPU's update O from the weight change (FP32 arithmetic:
-    # W' = W (1 - lr wd) - lr O).
-    lr, wd = np.float32(w.lr), np.float32(w.wd)
-    decay = np.float32(1.0) - lr * wd
-    O_gpu = (W.astype(np.float64) * float(decay) - Wg.astype(np.float64)) / float(lr)
-    Xb = o.bf16_rne(Mg)
-    transposed = Xb.shape[0] > Xb.shape[1]
-    X = Xb.T if transposed else Xb
-    Og = O_gpu.T if transposed else O_gpu
-    s = o.frobenius_scale(Mg)
-    dev_ = torch.device("cuda")
-    torch.backends.cuda.matmul.allow_tf32 = False   # true FP32 products
-    X0 = torch.from_numpy(X / s).to(dev_, torch.float32)
-    Ot = torch.from_numpy(Og).to(dev_, torch.float32)
-    # FP32 re-statement of the iteration on cuBLAS (not the library's kernels).
-    a, b, c = o.NS_COEFFS
-    Xk = X0.clone()
-    for _ in range(w.ns_steps):
-        A = Xk @ Xk.T
-        B = b * A + c * (A @ A)
-        Xk = a * Xk + B @ Xk
-    err = (torch.linalg.norm(Ot - Xk) / torch.linalg.norm(Xk)).item()
-    # O X0^T is a polynomial in A = X0 X0^T, hence symmetric.
-    S = Ot @ X0.T
-    asym = (torch.linalg.norm(S - S.T) / torch.linalg.norm(S)).item()
-    # The weight change carries FP32 rounding of W (1 - lr wd) ~ 6e-8 |W|,
-    # i.e. ~3e-6 |W| / lr relative to O; allow for it.
-    slack = 4e-6 * np.linalg.norm(W) / (w.lr * torch.linalg.norm(Xk).item())
-    assert err <= NS_TOL + slack, f"group {gi}: {err:.3e}"
-    assert asym <= NS_TOL + slack, f"group {gi}: asymmetry {asym:.3e}"
-
-
 def test_fullsize_l24_attention(ns):
-    # 96 x 2048^2: the benchmark's default workload.
+    # 96 x 2048^2 (rung L=24 attention).
     w, before, after = step_workload(ns, "l24_attention", [(0, 0), (0, 57), (0, 95)])
     for k in before:
         check_sample(w, before, after, k, model=(k == (0, 0)))
@@ -148,15 +108,14 @@ def test_fullsize_l48_model_layer(ns):
 
 
 def test_fullsize_l102_layer(ns):
-    # 226 GB of FP32 state.  Experts against the oracle; the 8704 x 13056
-    # shared expert and the 8704^2 attention through the size-free checks.
-    samples = [(0, 0), (1, 511), (0, 7)]
-    heavy = [(2, 0), (4, 3)]
-    w, before, after = step_workload(ns, "l102_layer", samples, heavy)
+    # 226 GB of FP32 state.  Experts of both orientations, the shared
+    # expert's tall 13056 x 8704 up-projection and an 8704 x 8704 attention
+    # projection against the FP64 oracle; those two and a transposed expert
+    # also against the error model.
+    samples = [(0, 0), (1, 511), (0, 7), (2, 0), (4, 3)]
+    w, before, after = step_workload(ns, "l102_layer", samples)
     for k in samples:
-        check_sample(w, before, after, k)
-    for k in heavy:
-        check_heavy(w, before, after, k)
+        check_sample(w, before, after, k, model=(k in ((2, 0), (4, 3), (1, 511))))
 
 
 def test_fullsize_l48_experts_variants(ns):
@@ -201,10 +160,13 @@ def test_fullsize_l48_experts_variants(ns):
         assert err <= bound, f"group {gi} matrix {i}: {err:.3e} vs error model {bound:.3e}"
 
 
-def test_fullsize_l24_host_buffers_match_device_step(ns):
-    """The end-to-end entry point at the benchmark's size: muon_step_host on
+@pytest.mark.parametrize("pinning", ["torch", "muon_host_alloc"])
+def test_fullsize_l24_host_buffers_match_device_step(ns, pinning):
+    """The end-to-end entry point at a benchmark size: muon_step_host on
     pinned host buffers (pipelined pieces, ramped first and last pieces)
-    gives the device-buffer step's weights and momenta bit for bit."""
+    gives the device-buffer step's weights and momenta bit for bit, with
+    torch's pinned memory and with the library's own page-locked
+    allocation."""
     from newton_schulz_03_gb300.workloads import WORKLOADS, make_group_torch
     w = WORKLOADS["l24_attention"]
     need = sum(g.numel for g in w.groups) * 12 + (9 << 30)
@@ -212,12 +174,17 @@ def test_fullsize_l24_host_buffers_match_device_step(ns):
         pytest.skip(f"needs {need / 2**30:.0f} GiB free on the device")
     groups = [(g.rows, g.cols, g.count) for g in w.groups]
     W, M, G = make_group_torch(w, 0, "cuda")
-    Wh, Mh, Gh = (t.cpu().pin_memory() for t in (W, M, G))
+    if pinning == "torch":
+        Wh, Mh, Gh = (t.cpu().pin_memory() for t in (W, M, G))
+    else:
+        Wh, Mh, Gh = (ns.host_empty(tuple(t.shape)) for t in (W, M, G))
+        for hst, dev in zip((Wh, Mh, Gh), (W, M, G)):
+            hst.copy_(dev)
     with ns.Handle() as h:
         ns.muon_step_host(h.value, groups, [Mh], [Gh], [Wh], w.lr, w.wd, w.mu, w.ns_steps)
         ns.muon_step(h.value, groups, [M], [G], [W], w.lr, w.wd, w.mu, w.ns_steps)
         ns.muon_last_device_error(h.value)
     assert torch.equal(Mh, M.cpu())
     assert torch.equal(Wh, W.cpu())
-    del W, M, G
+    del W, M, G, Wh, Mh, Gh
     torch.cuda.empty_cache()

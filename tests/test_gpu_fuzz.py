@@ -9,8 +9,12 @@ rules); every matrix of the result is compared with the oracle:
 * weights: the Newton-Schulz error, (|dW| - fp32 term) / (lr s |O|), within
   the BF16 error model -- 1.15 x the distance of the oracle's BF16
   emulation (rounding where the kernels store) from the exact iteration,
-  plus 5e-4.  A fixed bar does not hold over this range: with three rows,
-  or seven iterations, the format's own error exceeds 2e-2.
+  plus 5e-4;
+* and, for every matrix with at least 64 rows and columns run for at most
+  5 iterations, within the fixed 2e-2 relative Frobenius bar against the
+  exact FP64 iteration.  The fixed bar does not hold over the whole range:
+  with three rows, or seven iterations, the format's own error exceeds
+  2e-2, so smaller or longer cases are held to the error model alone.
 
 The update is W <- W(1 - lr wd) - lr s O (Frontier Pre-training at
 Microsoft AI, Method details §5, resharding step 5); the iteration is the
@@ -31,6 +35,7 @@ SCHED = [(4.0848, -6.8946, 2.9270), (3.9505, -6.3029, 2.6377), (3.7418, -5.5913,
          (2.8769, -3.1427, 1.2046), (2.8366, -3.0525, 1.2012)]
 LR, WD, MU = 0.02, 0.1, 0.95
 CALLS = 40
+NS_TOL = 2e-2
 
 
 @pytest.fixture(scope="module")
@@ -67,7 +72,7 @@ def draw_call(rng):
 @pytest.mark.parametrize("seed", list(range(11, 19)))
 def test_random_groups_within_error_model(ns, h, seed):
     rng = np.random.default_rng(seed)
-    checked = 0
+    checked = fixed = 0
     for _ in range(CALLS):
         groups, arrays, steps, nesterov, rule, sched = draw_call(rng)
         dW = [torch.from_numpy(a[0].copy()).cuda() for a in arrays]
@@ -98,5 +103,8 @@ def test_random_groups_within_error_model(ns, h, seed):
                 fp = 1e-6 * (np.linalg.norm(W[i]) + LR * abs(scale) * on)
                 err = (dw - fp) / (LR * abs(scale) * on)
                 assert err <= bound, f"{where}: error {err:.3e} > model bound {bound:.3e}"
+                if min(r, c) >= 64 and steps <= 5:
+                    assert err <= NS_TOL, f"{where}: error {err:.3e} > {NS_TOL}"
+                    fixed += 1
                 checked += 1
-    assert checked > 0
+    assert checked > 0 and fixed > 0
