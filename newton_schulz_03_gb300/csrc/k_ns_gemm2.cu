@@ -141,7 +141,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = pair; t < p.total_tiles && ok; t += npairs) {
         int mat, ti, tj;
-        decode_tile(p, MODE, kPairM, kPairN, t, mat, ti, tj);
+        decode_tile_banded(p, MODE, t, mat, ti, tj);
         const int rowA = ti * kPairM + static_cast<int>(rank) * kHalf;
         const int colB = tj * kPairN + static_cast<int>(rank) * kHalf;
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -220,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         int mat, ti, tj;
-        decode_tile(p, MODE, kPairM, kPairN, t, mat, ti, tj);
+        decode_tile_banded(p, MODE, t, mat, ti, tj);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kPairN);
         for (int kb = 0; kb < num_kb; ++kb) {
           const int kblk = (kb * kBK) / kPairM;
@@ -275,7 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int issued = 0;
     for (int t = pair; t < p.total_tiles; t += npairs) {
       int mat, ti, tj;
-      decode_tile(p, MODE, kPairM, kPairN, t, mat, ti, tj);
+      decode_tile_banded(p, MODE, t, mat, ti, tj);
       const int rb = ti * (kPairM / kBM) + static_cast<int>(rank);  // 128-row block index
       EpiAux<MODE, kPairN, false> aux;
       aux.start(p, mat, rb * kBM + r_tile, rb, tj * kPairN);   // loads overlap the MMAs
@@ -315,6 +315,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
+}
+
+// Row tiles per band of the tile order: the band's 256-row blocks of the
+// left operand (K elements each) should take about kBandBytes, so that
+// they stay in L2 while the band's columns go by; bands are then evened
+// out over the matrix's row tiles.
+constexpr double kBandBytes = 40.0 * (1 << 20);
+
+int band_rows(int tiles_m, int K) {
+  int g = static_cast<int>(kBandBytes / (double(kPairM) * K * 2.0));
+  if (g < 1) g = 1;
+  if (g > tiles_m) g = tiles_m;
+  const int bands = (tiles_m + g - 1) / g;
+  return (tiles_m + bands - 1) / bands;
 }
 
 template <int MODE>
@@ -376,6 +390,7 @@ cudaError_t ns_pair_gram(const CUtensorMap& tx, const CUtensorMap& tout, int m, 
   p.tiles_n = p.tiles_m;
   p.tiles_per_matrix = p.tiles_m * (p.tiles_m + 1) / 2;
   p.total_tiles = p.tiles_per_matrix * count;
+  p.group_rows = band_rows(p.tiles_m, p.K);
   p.out_cols = m;
   p.out = static_cast<__nv_bfloat16*>(const_cast<void*>(A_out.ptr));
   p.out_ld = A_out.ld;
@@ -397,6 +412,7 @@ cudaError_t ns_pair_poly(const CUtensorMap& ta, const CUtensorMap& ta_t, const C
   p.tiles_n = p.tiles_m;
   p.tiles_per_matrix = p.tiles_m * (p.tiles_m + 1) / 2;
   p.total_tiles = p.tiles_per_matrix * count;
+  p.group_rows = band_rows(p.tiles_m, p.K);
   p.out_cols = m;
   p.out = static_cast<__nv_bfloat16*>(const_cast<void*>(B_out.ptr));
   p.out_ld = B_out.ld;
@@ -424,6 +440,7 @@ cudaError_t ns_pair_update(const CUtensorMap& tb, const CUtensorMap& tb_t, const
   p.tiles_n = (n + kPairN - 1) / kPairN;
   p.tiles_per_matrix = p.tiles_m * p.tiles_n;
   p.total_tiles = p.tiles_per_matrix * count;
+  p.group_rows = band_rows(p.tiles_m, p.K);
   p.out_cols = n;
   p.out = static_cast<__nv_bfloat16*>(const_cast<void*>(X_out.ptr));
   p.out_ld = X_out.ld;

@@ -36,6 +36,7 @@ struct NsArgs {
   float c0, c1, c2;           // POLY: (b, c, a): B' = a I + b A + c A A
   int* err;
   int32_t mn4d;               // MN-major operand maps are 4-D chunk views (one copy per operand)
+  int32_t group_rows;         // pair kernels: row tiles per band of the tile order (>= 1)
 };
 
 // Tile t -> (matrix, row tile, column tile).  Symmetric products list, per
@@ -56,6 +57,55 @@ __device__ __forceinline__ void decode_tile(const NsArgs& p, int mode, int tile_
     }
     ti = i;
     tj = (i * tile_rows) / tile_cols + l;
+  }
+}
+
+// Tile order of the CTA-pair kernels (square 256 x 256 tiles): a matrix's
+// tiles go band by band, a band being `group_rows` consecutive row tiles,
+// and inside a band column by column (each column's rows in order).  The
+// pairs running at one time then share a few row blocks of the left
+// operand and a few column blocks of the right one, a working set that L2
+// holds, instead of sweeping a whole row of tiles -- and so the whole right
+// operand -- per row block.  Symmetric products list only the tiles
+// (i, j) with i <= j: column j of a band holds its rows up to j.
+__device__ __forceinline__ void decode_tile_banded(const NsArgs& p, int mode, int t, int& mat,
+                                                   int& ti, int& tj) {
+  mat = t / p.tiles_per_matrix;
+  int l = t - mat * p.tiles_per_matrix;
+  const int T = p.tiles_m, G = p.group_rows;
+  if (mode == kUpdate) {
+    const int band = l / (G * p.tiles_n);
+    const int r0 = band * G;
+    const int rows = min(G, T - r0);
+    l -= r0 * p.tiles_n;
+    tj = l / rows;
+    ti = r0 + (l - tj * rows);
+    return;
+  }
+  int r0 = 0;
+  for (;;) {
+    const int r1 = min(r0 + G, T);
+    const int k = r1 - r0;
+    const int tri = k * (k + 1) / 2;          // columns r0 .. r1-1: 1, 2, .., k rows
+    const int cnt = tri + (T - r1) * k;       // columns r1 .. T-1: k rows each
+    if (l < cnt) {
+      if (l < tri) {
+        int c = 1;
+        while (l >= c) {
+          l -= c;
+          ++c;
+        }
+        tj = r0 + c - 1;
+        ti = r0 + l;
+      } else {
+        l -= tri;
+        tj = r1 + l / k;
+        ti = r0 + (l - (l / k) * k);
+      }
+      return;
+    }
+    l -= cnt;
+    r0 = r1;
   }
 }
 
