@@ -81,7 +81,8 @@ typedef enum {
   MUON_KERNEL_APPLY = 5,          /* W = W (1 - lr wd) - lr s O */
   MUON_KERNEL_SCALE = 6,          /* ns_steps == 0: O = X / s */
   MUON_KERNEL_ADAMW = 7,          /* AdamW companion */
-  MUON_KERNEL_COUNT = 8
+  MUON_KERNEL_TRANSPOSE = 8,      /* BF16 transpose (resharded step) */
+  MUON_KERNEL_COUNT = 9
 } muon_kernel_t;
 
 typedef struct {
@@ -187,6 +188,62 @@ muon_status_t muon_step_host(muon_handle_t handle, const muon_group_t* groups, i
                              float* const* momentum_host, const float* const* grad_host,
                              float* const* weights_host, float lr, float wd, float mu,
                              int32_t ns_steps, void* stream);
+
+/* ------------------------------------------------------------------
+ * Resharded step (ZeRO data parallelism over several GPUs).
+ * "Frontier Pre-training at Microsoft AI", Method details §5, resharding
+ * pipeline steps 1-5, and "How to Make Parameter Updates Faster and More
+ * Stable?" ("batched momentum resharding"): each rank holds a flat shard
+ * of every group's FP32 momentum, gradient and weights; it updates and
+ * casts its momentum shard (step 1), an all-to-all per group gives every
+ * rank the complete matrices muon_partition assigns it (step 2), the owner
+ * orthogonalises them (step 3), a second all-to-all returns each shard's
+ * update (step 4), and each rank applies it to its weight shard (step 5).
+ * The exchanges themselves are collectives of the caller's communication
+ * library; these entry points are the local compute between them.  A
+ * shard is the element range [shard_begin, shard_end) of a group's flat
+ * buffer; matrix k occupies [k E, (k + 1) E) with E = rows * cols.
+ * ------------------------------------------------------------------ */
+
+/* Step 1 on a shard: M <- mu M + G in place (FP32, fused multiply-add, the
+ * same arithmetic as muon_step), x_shard <- bf16_rne(M) in the shard's
+ * flat layout, and sumsq_out[y] <- the sum of M^2 over the shard's piece
+ * of matrix shard_begin / E + y, for every matrix the shard touches
+ * ((shard_end - 1) / E - shard_begin / E + 1 entries; FP32 per block,
+ * FP64 across blocks, rounded to FP32).  momentum_shard, grad_shard:
+ * shard_end - shard_begin FP32 (device); x_shard: as many BF16 (device);
+ * sumsq_out: device FP32.  Uses the handle's workspace for the block
+ * partials.  Errors: INVALID_ARG, NOMEM, CUDA. */
+muon_status_t muon_shard_momentum_cast(muon_handle_t handle, int64_t shard_begin,
+                                       int64_t shard_end, int64_t matrix_elems,
+                                       float* momentum_shard, const float* grad_shard, float mu,
+                                       uint16_t* x_shard, float* sumsq_out, void* stream);
+
+/* On the owner of `count` whole wide matrices m x n (x_wide, BF16,
+ * contiguous): inv_norm[k] <- 1 / (sqrt(sum of sumsq[k * parts + j] over j)
+ * + 1e-7), the partial sums being the pieces' sums of squares gathered
+ * from the shards (parts per matrix, zero where a rank held no piece).
+ * As in muon_momentum_cast, a norm above 2^60 rescales x_wide by an exact
+ * power of two and inv_norm by its inverse; a non-finite norm sets the
+ * device error flag (MUON_ERR_NONFINITE).  Errors: INVALID_ARG, CUDA. */
+muon_status_t muon_norm_from_sumsq(muon_handle_t handle, int32_t m, int32_t n, int32_t count,
+                                   int32_t parts, const float* sumsq, uint16_t* x_wide,
+                                   float* inv_norm, void* stream);
+
+/* dst[k] <- src[k]^T for `count` BF16 matrices of rows x cols (both
+ * contiguous, device, not overlapping): the owner turns tall matrices wide
+ * for the Newton-Schulz products and the updates back.  Errors:
+ * INVALID_ARG (sizes as muon_step's groups, NULL, overlap), CUDA. */
+muon_status_t muon_transpose_bf16(muon_handle_t handle, int32_t rows, int32_t cols, int32_t count,
+                                  const uint16_t* src, uint16_t* dst, void* stream);
+
+/* Step 5 on a shard: W <- W (1 - lr wd) - lr scale fp32(O) over n_elems
+ * flat elements (the same arithmetic as muon_step's apply).
+ * weights_shard: FP32 in/out; o_shard: BF16 (device).  Errors:
+ * INVALID_ARG (n_elems < 0, NULL, non-finite scalars), CUDA. */
+muon_status_t muon_shard_apply(muon_handle_t handle, int64_t n_elems, float* weights_shard,
+                               const uint16_t* o_shard, float lr, float wd, float scale,
+                               void* stream);
 
 /* Page-locked host memory for the buffers of muon_step_host
  * (cudaHostAlloc, portable across devices).  Copies from it run at the

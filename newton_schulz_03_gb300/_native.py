@@ -22,7 +22,7 @@ STATUS_NAMES = {
     7: "MUON_ERR_NO_DEVICE",
 }
 KERNEL_NAMES = ("momentum_cast", "norm", "ns_gram", "ns_poly", "ns_update", "apply", "scale",
-                "adamw")
+                "adamw", "transpose")
 N_KERNELS = len(KERNEL_NAMES)
 
 # Symbols the header declares (checked by the CPU test-suite).
@@ -33,6 +33,7 @@ EXPORTED = (
     "muon_set_kernel_timing", "muon_kernel_stats", "muon_reset_kernel_stats",
     "muon_newton_schulz_bf16_static", "muon_selftest_bounded_wait", "muon_step_ex",
     "muon_adamw_step", "muon_partition", "muon_host_alloc", "muon_host_free",
+    "muon_shard_momentum_cast", "muon_norm_from_sumsq", "muon_transpose_bf16", "muon_shard_apply",
 )
 SCALE_NONE, SCALE_SQRT_ASPECT, SCALE_RMS_MATCH = 0, 1, 2
 
@@ -96,6 +97,12 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "muon_create": (c_int, [P(c_vp), c_i32, c_sz]),
         "muon_destroy": (c_int, [c_vp]),
         "muon_plan_describe": (c_int, [P(_Group), c_i32, c_i32, c_sz, P(_PlanInfo)]),
+        "muon_shard_momentum_cast": (c_int, [c_vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                             c_vp, c_vp, c_f, c_vp, c_vp, c_vp]),
+        "muon_norm_from_sumsq": (c_int, [c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp,
+                                         c_vp]),
+        "muon_transpose_bf16": (c_int, [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
+        "muon_shard_apply": (c_int, [c_vp, ctypes.c_int64, c_vp, c_vp, c_f, c_f, c_f, c_vp]),
         "muon_host_alloc": (c_int, [c_sz, P(c_vp)]),
         "muon_host_free": (c_int, [c_vp]),
         "muon_partition": (c_int, [P(_Group), c_i32, c_i32, c_i32, P(ctypes.c_int64), P(c_i32),
@@ -213,6 +220,31 @@ def muon_plan_describe(groups: Sequence[GroupLike], ns_steps: int = 5,
     _check(load_library().muon_plan_describe(_groups(groups), len(groups), ns_steps,
                                              workspace_bytes_max, ctypes.byref(info)))
     return {f: getattr(info, f) for f, _ in _PlanInfo._fields_}
+
+
+def muon_shard_momentum_cast(handle: int, shard_begin: int, shard_end: int, matrix_elems: int,
+                             momentum, grad, mu: float, x_shard, sumsq, stream=None) -> None:
+    _check(load_library().muon_shard_momentum_cast(handle, shard_begin, shard_end, matrix_elems,
+                                                   _ptr(momentum), _ptr(grad), mu, _ptr(x_shard),
+                                                   _ptr(sumsq), _stream(stream)))
+
+
+def muon_norm_from_sumsq(handle: int, m: int, n: int, count: int, parts: int, sumsq, x_wide,
+                         inv_norm, stream=None) -> None:
+    _check(load_library().muon_norm_from_sumsq(handle, m, n, count, parts, _ptr(sumsq),
+                                               _ptr(x_wide), _ptr(inv_norm), _stream(stream)))
+
+
+def muon_transpose_bf16(handle: int, rows: int, cols: int, count: int, src, dst,
+                        stream=None) -> None:
+    _check(load_library().muon_transpose_bf16(handle, rows, cols, count, _ptr(src), _ptr(dst),
+                                              _stream(stream)))
+
+
+def muon_shard_apply(handle: int, n_elems: int, weights, o_shard, lr: float, wd: float,
+                     scale: float = 1.0, stream=None) -> None:
+    _check(load_library().muon_shard_apply(handle, n_elems, _ptr(weights), _ptr(o_shard), lr, wd,
+                                           scale, _stream(stream)))
 
 
 def muon_host_alloc(nbytes: int) -> int:

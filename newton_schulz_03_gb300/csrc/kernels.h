@@ -63,6 +63,23 @@ cudaError_t launch_scale_bf16(int m, int n, int count, const uint16_t* x, int64_
                               int64_t x_ms, uint16_t* out, int64_t o_ld, int64_t o_ms,
                               const float* inv_norm, cudaStream_t stream);
 
+// ------------------------------------------------------------------ shards
+// Resharded step, on a rank's flat shard [begin, end) of a group whose
+// matrices have E elements: M <- mu M + G (in place), X <- bf16(M) (flat,
+// the shard's layout), and sums[y] = sum of M^2 over the shard's piece of
+// matrix begin/E + y (two-level: FP32 per block into `partials`, `blocks`
+// per piece, then FP64 per piece).
+int shard_cast_blocks(int64_t piece_elems);
+cudaError_t launch_shard_cast(int64_t begin, int64_t end, int64_t E, float* M, const float* G,
+                              float mu, uint16_t* X, float* partials, int blocks, float* sums,
+                              cudaStream_t stream);
+// W <- W (1 - lr wd) - lr scale O over n flat elements (O BF16).
+cudaError_t launch_shard_apply(int64_t n, float* W, const uint16_t* O, float lr, float wd,
+                               float scale, cudaStream_t stream);
+// dst[k] = src[k]^T for `count` BF16 matrices of rows x cols (contiguous).
+cudaError_t launch_transpose_bf16(int rows, int cols, int count, const uint16_t* src,
+                                  uint16_t* dst, cudaStream_t stream);
+
 // ------------------------------------------------------------------ NS GEMMs
 // A BF16 matrix batch: element pointer, row pitch and matrix pitch (elements).
 struct BatchView {

@@ -843,6 +843,87 @@ muon_status_t muon_step_host(muon_handle_t h, const muon_group_t* groups, int32_
   return MUON_OK;
 }
 
+muon_status_t muon_shard_momentum_cast(muon_handle_t h, int64_t shard_begin, int64_t shard_end,
+                                       int64_t matrix_elems, float* momentum_shard,
+                                       const float* grad_shard, float mu, uint16_t* x_shard,
+                                       float* sumsq_out, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  if (matrix_elems < 1 || shard_begin < 0 || shard_end < shard_begin)
+    return fail(MUON_ERR_INVALID_ARG, "need matrix_elems >= 1 and 0 <= shard_begin <= shard_end");
+  if (!std::isfinite(mu)) return fail(MUON_ERR_INVALID_ARG, "mu must be finite");
+  if (shard_end == shard_begin) return MUON_OK;
+  if (momentum_shard == nullptr || grad_shard == nullptr || x_shard == nullptr ||
+      sumsq_out == nullptr)
+    return fail(MUON_ERR_INVALID_ARG, "NULL buffer");
+  const int64_t pieces = (shard_end - 1) / matrix_elems - shard_begin / matrix_elems + 1;
+  const int blocks =
+      muon::shard_cast_blocks(std::min<int64_t>(matrix_elems, shard_end - shard_begin));
+  st = ensure_workspace(h, std::max(h->ws_size, align_up(size_t(pieces) * blocks * 4, kAlign)));
+  if (st != MUON_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchScope Ls(h, MUON_KERNEL_MOMENTUM_CAST, s);
+  cudaError_t e = muon::launch_shard_cast(shard_begin, shard_end, matrix_elems, momentum_shard,
+                                          grad_shard, mu, x_shard, static_cast<float*>(h->ws),
+                                          blocks, sumsq_out, s);
+  if (e != cudaSuccess) return cuda_fail(e, "shard cast launch");
+  return MUON_OK;
+}
+
+muon_status_t muon_norm_from_sumsq(muon_handle_t h, int32_t m, int32_t n, int32_t count,
+                                   int32_t parts, const float* sumsq, uint16_t* x_wide,
+                                   float* inv_norm, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  if (m < 1 || n < 1 || m > n || m > kMaxDim || n > kMaxDim || count < 0 || parts < 1)
+    return fail(MUON_ERR_INVALID_ARG, "need 1 <= m <= n <= 2^20, count >= 0, parts >= 1");
+  if (count == 0) return MUON_OK;
+  if (sumsq == nullptr || x_wide == nullptr || inv_norm == nullptr)
+    return fail(MUON_ERR_INVALID_ARG, "NULL buffer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchScope Ls(h, MUON_KERNEL_NORM, s);
+  cudaError_t e = muon::launch_norm_finalize(sumsq, parts, count, MUON_NORM_EPS, inv_norm,
+                                             h->dev_err, x_wide, n, int64_t(m) * n, m, n, s);
+  if (e != cudaSuccess) return cuda_fail(e, "norm launch");
+  return MUON_OK;
+}
+
+muon_status_t muon_transpose_bf16(muon_handle_t h, int32_t rows, int32_t cols, int32_t count,
+                                  const uint16_t* src, uint16_t* dst, void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  const muon_group_t g{rows, cols, count, 1.0f};
+  st = validate_groups(&g, 1);
+  if (st != MUON_OK) return st;
+  if (count == 0) return MUON_OK;
+  if (src == nullptr || dst == nullptr) return fail(MUON_ERR_INVALID_ARG, "NULL buffer");
+  const size_t bytes = size_t(count) * rows * cols * 2;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(dst);
+  if (a < b + bytes && b < a + bytes) return fail(MUON_ERR_INVALID_ARG, "src and dst overlap");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchScope Ls(h, MUON_KERNEL_TRANSPOSE, s);
+  cudaError_t e = muon::launch_transpose_bf16(rows, cols, count, src, dst, s);
+  if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
+  return MUON_OK;
+}
+
+muon_status_t muon_shard_apply(muon_handle_t h, int64_t n_elems, float* weights_shard,
+                               const uint16_t* o_shard, float lr, float wd, float scale,
+                               void* stream) {
+  muon_status_t st = check_handle(h);
+  if (st != MUON_OK) return st;
+  if (n_elems < 0) return fail(MUON_ERR_INVALID_ARG, "n_elems < 0");
+  if (!finite3(lr, wd, scale)) return fail(MUON_ERR_INVALID_ARG, "lr, wd, scale must be finite");
+  if (n_elems == 0) return MUON_OK;
+  if (weights_shard == nullptr || o_shard == nullptr)
+    return fail(MUON_ERR_INVALID_ARG, "NULL buffer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchScope Ls(h, MUON_KERNEL_APPLY, s);
+  cudaError_t e = muon::launch_shard_apply(n_elems, weights_shard, o_shard, lr, wd, scale, s);
+  if (e != cudaSuccess) return cuda_fail(e, "shard apply launch");
+  return MUON_OK;
+}
+
 muon_status_t muon_host_alloc(size_t bytes, void** out) {
   if (out == nullptr) return fail(MUON_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
