@@ -501,9 +501,10 @@ def e2e_passes(group_counts, elems_per_matrix, budget_bytes) -> int:
 
 
 # Pinned host footprint of the end-to-end leg.  On the GB300 hosts measured
-# here, copies from cudaHostAlloc memory ran at the link's ~210 GB/s up to
-# 16-32 GiB of it and slowed beyond; 20 GiB keeps the leg link-bound.
-E2E_HOST_BYTES = 20 << 30
+# here, copies from cudaHostAlloc memory ran at the link's ~200 GB/s each
+# way up to 16 GiB of it, and beyond 16-32 GiB (depending on the host) one
+# direction fell to 56-100 GB/s; 12 GiB keeps the leg at the link's rate.
+E2E_HOST_BYTES = 12 << 30
 
 
 def run_e2e(args, ns, h, w, share, Ws, Ms, Gs, world):
