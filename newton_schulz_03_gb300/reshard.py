@@ -36,7 +36,9 @@ this package's kernels on the GPU (``muon_shard_momentum_cast``,
 ``muon_norm_from_sumsq``, ``muon_transpose_bf16``,
 ``muon_newton_schulz_bf16``, ``muon_shard_apply``); the exchanges go
 through a ``comm`` object, ``TorchDistComm`` for ``torch.distributed``
-(NCCL on GPUs, gloo on CPUs).  Newton-Schulz on the owner needs both sides
+(NCCL on GPUs, gloo on CPUs), started asynchronously so that one group's
+exchanges overlap another group's Newton-Schulz products (the pages'
+cross-batch prefetch).  Newton-Schulz on the owner needs both sides
 of the matrix to be multiples of 8 (the products' 16-byte TMA pitch).
 """
 
@@ -122,17 +124,30 @@ class ReshardPlan:
         return e - b
 
 
+class _Done:
+    """Handle of an exchange that already completed."""
+
+    def wait(self) -> None:
+        return None
+
+
 class TorchDistComm:
-    """The two exchanges over torch.distributed (default process group)."""
+    """The exchanges over torch.distributed (default process group).  With
+    `async_op` the collective is only started and a handle with wait() is
+    returned (NCCL runs it on its own stream, ordered after the work
+    already queued on the caller's stream; wait() orders the caller's stream
+    after it)."""
 
-    def all_to_all(self, out, inp, out_splits, in_splits) -> None:
+    def all_to_all(self, out, inp, out_splits, in_splits, async_op: bool = False):
         import torch.distributed as dist
-        dist.all_to_all_single(out, inp, output_split_sizes=list(out_splits),
-                               input_split_sizes=list(in_splits))
+        work = dist.all_to_all_single(out, inp, output_split_sizes=list(out_splits),
+                                      input_split_sizes=list(in_splits), async_op=async_op)
+        return work if async_op else _Done()
 
-    def all_gather(self, out_list, inp) -> None:
+    def all_gather(self, out_list, inp, async_op: bool = False):
         import torch.distributed as dist
-        dist.all_gather(out_list, inp)
+        work = dist.all_gather(out_list, inp, async_op=async_op)
+        return work if async_op else _Done()
 
 
 def _bytes(t):
@@ -203,42 +218,40 @@ class LibraryOps:
 
 
 def resharded_step(plan: ReshardPlan, rank: int, state: Sequence, lr: float, wd: float,
-                   mu: float, ops, comm=None) -> None:
+                   mu: float, ops, comm=None, overlap: bool = True) -> None:
     """One Muon step of rank `rank`.  state[g] = (M, G, W) of this rank: 1-D
     FP32 tensors of the rank's shard of group g (its whole buffer for a
-    replicated group); M and W are updated in place."""
+    replicated group); M and W are updated in place.
+
+    With `overlap` (the pages' cross-batch prefetch) the exchanges are
+    started asynchronously: every group's first exchange is under way
+    before the first group is orthogonalised, and each group's return
+    exchange runs while the next groups are orthogonalised, so the
+    collectives of one group overlap the Newton-Schulz products of
+    another.  Every rank issues the collectives in the same order (group
+    by group), as the collectives require."""
     comm = comm or TorchDistComm()
     world = plan.world
     steps = plan.ns_steps
+    # Phase 1: shard-side update and cast; exchange 1 of every group started.
+    inbound = []
     for g, gl in enumerate(plan.groups):
         M, G, W = state[g]
-        E, r, c = gl.elems, gl.rows, gl.cols
-        first, own = gl.own[rank]
+        E = gl.elems
         if gl.replicated:
-            # Replicated: the whole momentum is here (no first exchange).
+            # The whole momentum is here (no first exchange).
             X, sums = ops.shard_cast(M, G, mu, 0, gl.total, E)
-            Xo = X[first * E:(first + own) * E].view(own, r, c)
-            So = sums[first:first + own].view(own, 1)
-            Oo = ops.orthogonalise(Xo, So, r, c, steps)
-            # One all-gather of the owners' updates (padded to the largest slice).
-            most = max(cnt for _, cnt in gl.own) * E
-            buf = ops.zeros(most, Oo.dtype, X)
-            if own:
-                buf[:own * E] = Oo.reshape(-1)
-            parts = [ops.empty(most, Oo.dtype, X) for _ in range(world)]
-            comm.all_gather([_bytes(p) for p in parts], _bytes(buf))
-            O = ops.empty(gl.total, Oo.dtype, X)
-            for p, (f, cnt) in enumerate(gl.own):
-                O[f * E:(f + cnt) * E] = parts[p][:cnt * E]
-            ops.apply(W, O, lr, wd, gl.scale)
+            inbound.append((X, sums, None, []))
             continue
         b, e = gl.shard[rank]
         X, sums = ops.shard_cast(M, G, mu, b, e, E)
-        # Exchange 1: pieces of X to the owners of their matrices.
+        first, own = gl.own[rank]
+        # Pieces of X to the owners of their matrices.
         Xown = ops.empty(own * E, X.dtype, X)
         isz = X.element_size()
-        comm.all_to_all(_bytes(Xown), _bytes(X), [gl.send[q][rank] * isz for q in range(world)],
-                        [gl.send[rank][p] * isz for p in range(world)])
+        w1 = comm.all_to_all(_bytes(Xown), _bytes(X),
+                             [gl.send[q][rank] * isz for q in range(world)],
+                             [gl.send[rank][p] * isz for p in range(world)], async_op=overlap)
         # The pieces' sums of squares go with them: rank q sends p the sums
         # of the matrices of p's slice that q's shard touches.
         k0 = gl.touched[rank][0]
@@ -252,18 +265,59 @@ def resharded_step(plan: ReshardPlan, rank: int, state: Sequence, lr: float, wd:
             at += hi - lo
         recv_sums = ops.empty(sum(out_n), sums.dtype, X)
         ssz = sums.element_size()
-        comm.all_to_all(_bytes(recv_sums), _bytes(send_sums), [n * ssz for n in out_n],
-                        [n * ssz for n in in_n])
-        S = ops.zeros((own, world), sums.dtype, X)
+        w2 = comm.all_to_all(_bytes(recv_sums), _bytes(send_sums), [n * ssz for n in out_n],
+                             [n * ssz for n in in_n], async_op=overlap)
+        inbound.append((X, send_sums, (Xown, recv_sums), [w1, w2]))
+    # Phase 2: orthogonalise each group as its pieces arrive; start its return.
+    outbound = []
+    for g, gl in enumerate(plan.groups):
+        E, r, c = gl.elems, gl.rows, gl.cols
+        first, own = gl.own[rank]
+        X, _, recv, works = inbound[g]
+        for w in works:
+            w.wait()
+        if gl.replicated:
+            sums = inbound[g][1]
+            Xo = X[first * E:(first + own) * E].view(own, r, c)
+            So = sums[first:first + own].view(own, 1)
+            Oo = ops.orthogonalise(Xo, So, r, c, steps)
+            # One all-gather of the owners' updates (padded to the largest slice).
+            most = max(cnt for _, cnt in gl.own) * E
+            buf = ops.zeros(most, Oo.dtype, X)
+            if own:
+                buf[:own * E] = Oo.reshape(-1)
+            parts = [ops.empty(most, Oo.dtype, X) for _ in range(world)]
+            w = comm.all_gather([_bytes(p) for p in parts], _bytes(buf), async_op=overlap)
+            outbound.append((parts, buf, w))
+            continue
+        Xown, recv_sums = recv
+        S = ops.zeros((own, world), recv_sums.dtype, X)
         at = 0
         for q in range(world):
             lo, hi = gl.sums_range(q, rank)
             if hi > lo:
                 S[lo - first:hi - first, q] = recv_sums[at:at + hi - lo]
             at += hi - lo
-        # Step 3 on the owner; exchange 2 returns each shard's update.
         O = ops.orthogonalise(Xown.view(own, r, c), S, r, c, steps)
+        b, e = gl.shard[rank]
         Oshard = ops.empty(e - b, O.dtype, X)
-        comm.all_to_all(_bytes(Oshard), _bytes(O), [gl.send[rank][p] * isz for p in range(world)],
-                        [gl.send[q][rank] * isz for q in range(world)])
+        isz = O.element_size()
+        w = comm.all_to_all(_bytes(Oshard), _bytes(O),
+                            [gl.send[rank][p] * isz for p in range(world)],
+                            [gl.send[q][rank] * isz for q in range(world)], async_op=overlap)
+        outbound.append((Oshard, O, w))
+    # Phase 3: apply each shard's update once it is back.
+    for g, gl in enumerate(plan.groups):
+        M, G, W = state[g]
+        E = gl.elems
+        if gl.replicated:
+            parts, _, w = outbound[g]
+            w.wait()
+            O = ops.empty(gl.total, parts[0].dtype, parts[0])
+            for p, (f, cnt) in enumerate(gl.own):
+                O[f * E:(f + cnt) * E] = parts[p][:cnt * E]
+            ops.apply(W, O, lr, wd, gl.scale)
+            continue
+        Oshard, _, w = outbound[g]
+        w.wait()
         ops.apply(W, Oshard, lr, wd, gl.scale)

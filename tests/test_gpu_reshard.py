@@ -94,7 +94,11 @@ class ThreadComm:
         self.slots = [None] * world
         self.local = threading.local()
 
-    def all_to_all(self, out, inp, out_splits, in_splits):
+    class _Done:
+        def wait(self):
+            return None
+
+    def all_to_all(self, out, inp, out_splits, in_splits, async_op=False):
         r = self.local.rank
         self.slots[r] = (inp, list(in_splits))
         self.bar.wait()
@@ -107,8 +111,9 @@ class ThreadComm:
             at += n
         torch.cuda.synchronize()
         self.bar.wait()
+        return self._Done()
 
-    def all_gather(self, out_list, inp):
+    def all_gather(self, out_list, inp, async_op=False):
         r = self.local.rank
         self.slots[r] = (inp, None)
         self.bar.wait()
@@ -116,6 +121,7 @@ class ThreadComm:
             out_list[q].copy_(self.slots[q][0])
         torch.cuda.synchronize()
         self.bar.wait()
+        return self._Done()
 
 
 GROUPS = [(256, 128, 3, 1.0), (128, 256, 5, 0.5), (512, 512, 2, 1.0), (64, 256, 2, 1.0),

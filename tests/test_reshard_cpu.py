@@ -100,7 +100,7 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, mode, out):
+def _worker(rank, world, port, mode, out, overlap=True):
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -108,18 +108,18 @@ def _worker(rank, world, port, mode, out):
     plan = ReshardPlan(GROUPS, world, replicated=REPLICATED, ns_steps=STEPS)
     state = _shards(plan, rank, _data())
     ops = OracleOps() if mode == "oracle" else IdentityOps()
-    resharded_step(plan, rank, state, HP["lr"], HP["wd"], HP["mu"], ops)
+    resharded_step(plan, rank, state, HP["lr"], HP["wd"], HP["mu"], ops, overlap=overlap)
     out[rank] = [(M.numpy().copy(), W.numpy().copy()) for M, _, W in state]
     dist.barrier()
     dist.destroy_process_group()
 
 
-def _run(world, mode):
+def _run(world, mode, overlap=True):
     import torch.multiprocessing as mp
     ctx = mp.get_context("spawn")
     mgr = ctx.Manager()
     out = mgr.dict()
-    mp.start_processes(_worker, args=(world, _free_port(), mode, out), nprocs=world,
+    mp.start_processes(_worker, args=(world, _free_port(), mode, out, overlap), nprocs=world,
                        start_method="spawn", join=True)
     return dict(out)
 
@@ -137,9 +137,11 @@ def _merge(ns, world, got, g):
     return tuple(np.concatenate([got[r][g][i] for r in range(world)]) for i in (0, 1))
 
 
-@pytest.mark.parametrize("world", [2, 3])
-def test_resharded_step_equals_the_one_rank_oracle_step(ns, world):
-    got = _run(world, "oracle")
+@pytest.mark.parametrize("world,overlap", [(2, True), (3, True), (2, False)])
+def test_resharded_step_equals_the_one_rank_oracle_step(ns, world, overlap):
+    # overlap: exchanges started asynchronously (one group's collectives
+    # beside another group's Newton-Schulz step); else one after the other.
+    got = _run(world, "oracle", overlap)
     data = _data()
     for g, (r, c, k, scale) in enumerate(GROUPS):
         M, W = _merge(ns, world, got, g)
