@@ -164,14 +164,6 @@ class LibraryOps:
         self.h = handle
         self.stream = stream
 
-    def payload_dtype(self):
-        import torch
-        return torch.int16
-
-    def sums_dtype(self):
-        import torch
-        return torch.float32
-
     def empty(self, n, dtype, like):
         import torch
         return torch.empty(n, dtype=dtype, device=like.device)

@@ -15,7 +15,7 @@ transpose, so an up/down pair shares one Newton-Schulz batch.
 
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 from typing import Dict, List, Optional, Tuple
 
 import numpy as np
