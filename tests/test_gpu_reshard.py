@@ -193,3 +193,73 @@ def test_resharded_step_with_the_library_matches_the_one_gpu_step(ns, world):
             step_single = (W0[sl].double() * (1 - HP["lr"] * HP["wd"]) - Ws[sl].double())
             diff = (W[sl].double() - Ws[sl].double()).norm().item()
             assert diff <= 1e-2 * step_single.norm().item() + 1e-7, f"group {g} matrix {i}"
+
+
+def test_resharded_step_at_full_size_matches_the_one_gpu_step(ns):
+    """The L=48 expert workload (1024 matrices, 77 GB of FP32 state) over
+    two thread ranks: each rank's shard of a group holds 1.6e9 elements and
+    rank 1's shard spans global offsets up to 3.2e9 (beyond 2^31, in the
+    shard kernels' piece arithmetic), and the exchanges move whole
+    1536 x 4096 matrices.  Sampled matrices: momenta bit for bit, weights
+    within 1% of the update, against muon_step on the same data."""
+    from newton_schulz_03_gb300.reshard import LibraryOps, ReshardPlan, resharded_step
+    from newton_schulz_03_gb300.workloads import WORKLOADS, make_group_torch
+    w = WORKLOADS["l48_experts"]
+    free, _ = torch.cuda.mem_get_info()
+    need = sum(g.numel for g in w.groups) * (12 + 12 + 12) + (16 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free on the device")
+    world = 2
+    groups = [(g.rows, g.cols, g.count) for g in w.groups]
+    plan = ReshardPlan(groups, world, ns_steps=w.ns_steps)
+    full = [make_group_torch(w, gi, "cuda") for gi in range(len(w.groups))]
+    samples = [(0, 0), (0, 7), (0, 300), (1, 511), (1, 256)]
+    W0 = {k: full[k[0]][0][k[1]].clone() for k in samples}
+    states = []
+    for rank in range(world):
+        st = []
+        for g, gl in enumerate(plan.groups):
+            b, e = gl.shard[rank]
+            W, M, G = (t.reshape(-1)[b:e].clone() for t in full[g])
+            st.append((M, G, W))
+        states.append(st)
+    handles = [ns.Handle() for _ in range(world)]
+    ns.muon_step(handles[0].value, groups, [t[1] for t in full], [t[2] for t in full],
+                 [t[0] for t in full], w.lr, w.wd, w.mu, w.ns_steps)
+    ns.muon_last_device_error(handles[0].value)
+    torch.cuda.synchronize()
+    comm = ThreadComm(world)
+    errors = []
+
+    def run(rank):
+        try:
+            comm.local.rank = rank
+            resharded_step(plan, rank, states[rank], w.lr, w.wd, w.mu,
+                           LibraryOps(handles[rank].value), comm)
+            torch.cuda.synchronize()
+            ns.muon_last_device_error(handles[rank].value)
+        except BaseException as exc:   # noqa: BLE001 -- reported below
+            errors.append(exc)
+            comm.bar.abort()
+
+    threads = [threading.Thread(target=run, args=(r,)) for r in range(world)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=600)
+    for h in handles:
+        h.close()
+    assert not errors, errors
+    for gi, i in samples:
+        gl = plan.groups[gi]
+        E = gl.elems
+        lo = i * E
+        M = torch.cat([states[q][gi][0] for q in range(world)])[lo:lo + E]
+        W = torch.cat([states[q][gi][2] for q in range(world)])[lo:lo + E]
+        assert torch.equal(M, full[gi][1][i].reshape(-1)), f"group {gi} matrix {i}: momentum"
+        Ws = full[gi][0][i].reshape(-1).double()
+        step = W0[(gi, i)].reshape(-1).double() * (1 - w.lr * w.wd) - Ws
+        diff = (W.double() - Ws).norm().item()
+        assert diff <= 1e-2 * step.norm().item() + 1e-7, f"group {gi} matrix {i}: weights"
+    del full, states
+    torch.cuda.empty_cache()
