@@ -514,7 +514,7 @@ muon_status_t muon_partition(const muon_group_t* groups, int32_t n_groups, int32
       const int64_t c = per[size_t(g) * world + r];
       first_out[size_t(g) * world + r] = first;
       count_out[size_t(g) * world + r] = static_cast<int32_t>(c);
-      load[r] += c * cost[g];
+      load[r] += static_cast<double>(c) * cost[g];
       first += c;
     }
   }
