@@ -84,25 +84,40 @@ def barrier(world: int) -> None:
         dist.barrier()
 
 
-def timed_steps(step, steps: int, warmup: int, world: int, stream, sync) -> float:
+def timed_steps(step, steps: int, warmup: int, world: int, stream, sync, per_step=None) -> float:
     """W untimed steps, then K steps between barrier+sync on both sides,
-    timed with CUDA events on `stream`.  Returns seconds (max over ranks)."""
+    timed with CUDA events on `stream`.  Returns seconds (max over ranks).
+    With a list `per_step`, an event is also recorded after every step and
+    the K step durations (ms, this rank) are appended to it; the total is
+    still the first event to the last."""
     import torch
     for _ in range(warmup):
         step()
     sync()
     barrier(world)
     sync()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True)
+          for _ in range(steps + 1 if per_step is not None else 2)]
+    ev[0].record(stream)
+    for i in range(steps):
         step()
-    e1.record(stream)
+        if per_step is not None:
+            ev[i + 1].record(stream)
+    ev[-1].record(stream)
     sync()
     barrier(world)
-    secs = e0.elapsed_time(e1) / 1e3
+    secs = ev[0].elapsed_time(ev[-1]) / 1e3
+    if per_step is not None:
+        per_step.extend(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
     return max_over_ranks(secs, world, device=torch.device("cuda", torch.cuda.current_device()))
+
+
+def step_count(t1: float) -> int:
+    """Default K from one step's time: about 5 s of steps (enough clock
+    samples), at least 10 steps (3 when a step takes over 0.6 s), at most
+    100."""
+    k = math.ceil(5.0 / max(t1, 1e-6))
+    return int(max(10 if t1 <= 0.6 else 3, min(100, k)))
 
 
 class ClockSampler:
@@ -295,15 +310,17 @@ def run_ours(args, world, rank, local):
     sync = torch.cuda.synchronize
     step()
     ns.muon_last_device_error(h, stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    step()
+    b.record(stream)
+    sync()
+    t1 = max_over_ranks(a.elapsed_time(b) / 1e3, world, device=torch.device(dev))
     if args.steps is None:
-        # Default K: about 1.5 s per timed pass (enough clock samples), 3..100.
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        step()
-        b.record(stream)
-        sync()
-        t1 = max_over_ranks(a.elapsed_time(b) / 1e3, world, device=torch.device(dev))
-        args.steps = int(max(3, min(100, math.ceil(1.5 / max(t1, 1e-6)))))
+        args.steps = step_count(t1)
+    # Per-step events break launch chaining at one kernel boundary per
+    # step: a few microseconds, nothing against steps of 1 ms or more.
+    per_step = [] if t1 >= 1e-3 else None
     ns.muon_reset_kernel_stats(h)
     graph_ms = None
     if args.graph:
@@ -322,7 +339,7 @@ def run_ours(args, world, rank, local):
         # The step as a user runs it: no per-kernel events.
         ns.muon_reset_kernel_stats(h)
         launches0 = ns.muon_kernel_stats(h)["total_launches"]
-        secs = timed_steps(step, args.steps, args.warmup, world, stream, sync)
+        secs = timed_steps(step, args.steps, args.warmup, world, stream, sync, per_step)
         launches1 = ns.muon_kernel_stats(h)["total_launches"]
         # The same K steps again with an event pair around every launch on
         # the launching stream: per-kernel durations for the roofline.  The
@@ -420,6 +437,9 @@ def run_ours(args, world, rank, local):
         "gpu_launches": gpu_launches,
         "graph_replay_ms_per_step": round(graph_ms, 4) if graph_ms is not None else None,
         "ms_per_step_with_kernel_events": round(secs_ev * 1e3 / args.steps, 4),
+        "ms_per_step_median": round(statistics.median(per_step), 4) if per_step else None,
+        "ms_per_step_min_max": [round(min(per_step), 4), round(max(per_step), 4)]
+        if per_step else None,
         "programmatic_dependent_launch": os.environ.get("MUON_PDL", "1") != "0",
         "clocks": clocks,
         "roofline": roofline,
@@ -721,7 +741,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: about 1.5 s of steps, 3 to 100)")
+                    help="timed steps (default: about 5 s of steps, 10 to 100; 3 when a step "
+                         "takes over 0.6 s)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

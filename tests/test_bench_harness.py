@@ -164,3 +164,14 @@ def test_oracle_rate_weights_groups_by_count():
     assert bench.workload_rate(w, {(64, 128): 1.0, (128, 256): 2.0}) == pytest.approx(9 / 12)
     per, done, secs = bench.oracle_shape_seconds(w, 1)
     assert set(per) == {(64, 128), (128, 256)} and done == 2 and secs > 0
+
+
+def test_default_step_count():
+    """About 5 s of steps: 10 to 100, or 3 when one step takes over 0.6 s."""
+    import bench
+    assert bench.step_count(7e-5) == 100          # tiny
+    assert bench.step_count(0.012) == 100         # l24
+    assert bench.step_count(0.133) == 38          # l48 experts
+    assert bench.step_count(0.49) == 11           # L=102 layer
+    assert bench.step_count(0.6) == 10
+    assert bench.step_count(6.7) == 3             # 48-layer model

@@ -49,3 +49,20 @@ def test_bench_json_line_contract():
     assert e["d2h_bytes_per_step"] == 4 * 128 * 64 * 8
     c = d["clocks"]
     assert "sm_mhz" in c and "sm_max_mhz" in c and isinstance(c["reasons"], list)
+    # Steps under 1 ms are timed as a block only (no per-step events).
+    assert d["ms_per_step_median"] is None and d["ms_per_step_min_max"] is None
+
+
+def test_bench_reports_the_median_step():
+    """Steps of 1 ms or more: an event after every step gives the median
+    and the extremes of the K step times beside the block time."""
+    r = subprocess.run([sys.executable, "bench.py", "--workload", "l24_attention",
+                        "--max-count", "16", "--steps", "10", "--warmup", "3", "--skip-e2e",
+                        "--skip-cpu-baseline"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.strip()][-1])
+    lo, hi = d["ms_per_step_min_max"]
+    assert 0 < lo <= d["ms_per_step_median"] <= hi
+    # The block time per step is the mean of the same K steps.
+    assert lo * 0.999 <= d["ms_per_step"] <= hi * 1.001
