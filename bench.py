@@ -401,6 +401,8 @@ def run_ours(args, world, rank, local):
         "ns_engine_frac": sig(ns_tflops / burst) if ns_tflops else None,
         "ns_engine_frac_of_sustained": sig(ns_tflops / sustained) if ns_tflops else None,
         "kernel_time_share": kernel_share,
+        "kernel_avg_launch_ms": {k: sig(stats["total_ms"][k] / n)
+                                 for k, n in stats["launches"].items() if n > 0},
     }
     # The HBM-bound kernels against the measured copy bandwidth: 14 B per
     # element for the momentum update + cast (read M, G; write M, X) and

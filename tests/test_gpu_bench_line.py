@@ -40,6 +40,10 @@ def test_bench_json_line_contract():
                                                     rel=1e-3)
     assert rf["achieved"] == pytest.approx(rf["flops_per_launch"] / (rf["avg_launch_ms"] * 1e9),
                                            rel=1e-4)
+    # Every kernel's average launch time from the same event pass.
+    assert rf["kernel_avg_launch_ms"]["ns_update"] == pytest.approx(rf["avg_launch_ms"], rel=1e-4)
+    assert set(rf["kernel_avg_launch_ms"]) >= {"momentum_cast", "ns_gram", "ns_poly", "ns_update",
+                                                "apply"}
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
     e = d["e2e"]
