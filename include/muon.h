@@ -316,7 +316,9 @@ muon_status_t muon_momentum_cast(muon_handle_t handle, int32_t rows, int32_t col
  * mirrored, and a consumer reads a block left of the diagonal as the
  * transpose of the stored block above it; for m <= 128 the matrix is one
  * tile, computed once and stored in full (the part above the diagonal
- * also written mirrored below it).
+ * also written mirrored below it).  MUON_NS_PAIR=0 in the environment
+ * runs every size on the single-CTA kernels (128-row tiles, stored in
+ * full), for comparisons.
  * x_dev, out_dev: count*m*n BF16, 16-byte aligned, must not overlap.
  * inv_norm_dev:   count FP32 (device).
  * coeffs_host:    3 floats (a, b, c) or NULL for the defaults.

@@ -1,7 +1,8 @@
 // ns_common.cuh -- pieces shared by the Newton-Schulz product kernels:
-// argument block, tile decoding, and the fused epilogue (TMEM -> registers
-// -> polynomial combine -> BF16 -> global, with mirrored stores for the
-// symmetric products).
+// argument block, tile decoding, and the fused epilogues (TMEM -> registers
+// -> polynomial combine -> BF16 -> global): direct stores, mirrored for the
+// symmetric products, in the single-CTA kernels; TMA stores of the upper
+// 256-block triangle in the CTA-pair kernels.
 #pragma once
 
 #include <cuda.h>
