@@ -177,7 +177,21 @@ class ClockSampler:
         reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v == "Active"})
         return {"sm_mhz": statistics.median(r[0] for r in loaded),
                 "sm_max_mhz": max(r[1] for r in rows), "power_w_max": max(r[2] for r in rows),
+                "power_w_median": statistics.median(r[2] for r in loaded),
                 "samples": len(loaded), "reasons": reasons}
+
+
+def energy_of_step(clocks: dict, ms_per_step: float, flops_step: float):
+    """Energy per step from the board power sampled during the timed passes
+    (median of the samples under load): the products run at the power cap,
+    so flops per joule is what bounds their throughput there."""
+    w = clocks.get("power_w_median")
+    if not w or ms_per_step <= 0:
+        return None
+    joules = w * ms_per_step / 1e3
+    return {"power_w_median": round(w, 1), "joules_per_step": sig(joules),
+            "tflop_per_joule": sig(flops_step / 1e12 / joules) if joules > 0 else None,
+            "source": "nvidia-smi power.draw every 200 ms during the timed passes"}
 
 
 def load_peaks():
@@ -444,6 +458,7 @@ def run_ours(args, world, rank, local):
         if per_step else None,
         "programmatic_dependent_launch": os.environ.get("MUON_PDL", "1") != "0",
         "clocks": clocks,
+        "energy": energy_of_step(clocks, ms_per_step, flops_step),
         "roofline": roofline,
         "hbm_kernels": hbm_kernels,
     }

@@ -175,3 +175,11 @@ def test_default_step_count():
     assert bench.step_count(0.49) == 11           # L=102 layer
     assert bench.step_count(0.6) == 10
     assert bench.step_count(6.7) == 3             # 48-layer model
+
+
+def test_energy_of_a_step():
+    import bench
+    e = bench.energy_of_step({"power_w_median": 1400.0}, 500.0, 7.0e14)
+    assert e["joules_per_step"] == 700.0
+    assert e["tflop_per_joule"] == pytest.approx(1.0)
+    assert bench.energy_of_step({"sm_mhz": None}, 500.0, 7.0e14) is None

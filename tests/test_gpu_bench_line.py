@@ -53,6 +53,10 @@ def test_bench_json_line_contract():
     assert e["d2h_bytes_per_step"] == 4 * 128 * 64 * 8
     c = d["clocks"]
     assert "sm_mhz" in c and "sm_max_mhz" in c and isinstance(c["reasons"], list)
+    en = d["energy"]
+    if en is not None:      # None only when nvidia-smi gave no samples
+        assert en["joules_per_step"] == pytest.approx(
+            en["power_w_median"] * d["ms_per_step"] / 1e3, rel=1e-3)
     # Steps under 1 ms are timed as a block only (no per-step events).
     assert d["ms_per_step_median"] is None and d["ms_per_step_min_max"] is None
 
